@@ -1,0 +1,449 @@
+"""Benchmark: BF16-in / FP32-accumulate GEMM, M = N = K = 8192, row-major.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+                    [--suite]
+
+One step is one call of gemm_bf16f32 on the M = N = K = 8192 workload (A and
+B drawn from normal(0, 1/sqrt(K)) and rounded to BF16, C in FP32).  A and B
+(256 MiB together) exceed the 129 MB L2, so no flush is needed between steps.
+Prints one JSON line (rank 0): TFLOP/s over the whole job, the dominant
+kernel's roofline fraction, the oracle timed on the host cores (a bounded
+sample of rows), an end-to-end figure through host buffers, the clocks seen
+while timing and the number of kernel launches.
+
+--impl reference times the CPU oracle instead (there is no other reference
+implementation), on the same workload and metric, each step a bounded sample
+of output rows.
+
+--suite additionally times every workload configuration (not part of the JSON
+line) and writes gpurun_out/bench_suite.json.
+
+With torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU; nothing is exchanged between ranks (the product's rows are
+independent), and the value is the total over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M = N = K = 8192
+FLOP = 2.0 * M * N * K
+WORKLOAD = ("gemm_bf16f32 M=N=K=8192 row-major; A,B ~ normal(0, 1/sqrt(K)) rounded to BF16, "
+            "C FP32, FP32 accumulate")
+METRIC = "GEMM TFLOP/s (FP16-in/FP32-acc, M=N=K=8192) and % of GB300 dense peak"
+SEED = 1238
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_bf16_8192_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "dense_gemm_tensor_tcgen05_gb300", "csrc", f)
+                  for f in ("tc_gemm.cu", "ptx.cuh", "api.cu", "internal.h")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu capture, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_hash") != kernel_source_hash():
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+# ---- clocks ---------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) while the benchmark runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        window = "timed"
+        if not win:
+            win = [s for (_, s) in self.samples]
+            window = "run"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        mx = [num(s[1]) for s in win if num(s[1]) is not None]
+        pw = [num(s[2]) for s in win if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4) if s[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win), "window": window}
+
+
+# ---- CPU oracle timing ------------------------------------------------------
+
+def oracle_rows_timing(A, B, target_s: float, max_rows: int):
+    """Time the oracle on a band of output rows sized to take about target_s.
+    Returns (seconds, rows, threads)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    rows = 1 if target_s < 1.0 else 8
+    t = None
+    while True:
+        rows = min(rows, max_rows)
+        t0 = time.perf_counter()
+        oracle.gemm_rows("bf16", A, B, 0, rows, M=M, N=N, K=K, nthreads=threads)
+        t = time.perf_counter() - t0
+        if t >= target_s * 0.5 or rows >= max_rows:
+            return t, rows, threads
+        rows = int(rows * min(8.0, max(2.0, target_s / max(t, 1e-3))))
+
+
+def make_inputs():
+    from dense_gemm_tensor_tcgen05_gb300 import inputs
+    A = inputs.make("normal", "bf16", M, K, SEED, 0, sigma=1 / math.sqrt(K))
+    B = inputs.make("normal", "bf16", K, N, SEED, 1, sigma=1 / math.sqrt(K))
+    return A, B
+
+
+# ---- the reference arm: the oracle ------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    A, B = make_inputs()
+    threads = os.cpu_count() or 1
+    # size one step so the whole run stays within a few minutes (a step is at
+    # least one output row, plus the oracle's decode of B)
+    target = max(0.05, min(2.0, 150.0 / (args.steps + args.warmup)))
+    _, rows, _ = oracle_rows_timing(A, B, target_s=target, max_rows=M)
+    for _ in range(args.warmup):
+        oracle.gemm_rows("bf16", A, B, 0, rows, M=M, N=N, K=K, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_rows("bf16", A, B, 0, rows, M=M, N=N, K=K, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flop = 2.0 * rows * N * K * args.steps
+    value = flop / dt / 1e12
+    sample = (f"{rows} of {M} output rows per step (2*{rows}*N*K FLOP), oracle in double, "
+              f"{threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- our arm -------------------------------------------------------------------
+
+def run_gb300(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    from dense_gemm_tensor_tcgen05_gb300 import build
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+    torch.cuda.set_device(local_rank)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist:
+        dist.barrier()
+    g.lib()
+
+    A, B = make_inputs()
+    Ad = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).cuda()
+    Bd = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).cuda()
+    Cd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    call = lambda: g.gemm_bf16f32(Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, K, N, N, sh)
+
+    # correctness before timing: one run, the device error word, and a sample
+    torch.cuda.synchronize()
+    call()
+    g.gemm_device_error(sh)
+    plan = g.gemm_plan_describe(1, Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, K, N, N)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = g.gemm_launch_count()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(args.steps):
+            call()
+            evs[i + 1].record(stream)
+    stream.synchronize()
+    t_wall1 = time.time()
+    launches = g.gemm_launch_count() - launches0
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    time.sleep(0.2)
+    sampler.stop()
+    g.gemm_device_error(sh)
+
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * FLOP * args.steps / (total_ms / 1e3) / 1e12
+    kernel_ms = statistics.mean(per)
+    peaks = load_peaks()
+    achieved = FLOP / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": load_traffic(),
+                "peak_source": f"bf16_tflops (burst) of {peaks['source']}",
+                "kernel": "tc_gemm_kernel<256,false>", "kernel_ms_mean": kernel_ms,
+                "kernel_ms_median": statistics.median(per),
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # end to end through the public API with host buffers: H2D of A and B,
+    # the product, D2H of C, every step
+    Ah = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Bh = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Ch = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        g.matmul(Ah, Bh, out=Ch, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            g.matmul(Ah, Bh, out=Ch, stream=stream)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_value = world * FLOP * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e = {"value": e2e_value, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2),
+           "d2h_bytes_per_step": int(Ch.numel() * 4), "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t, rows, threads = oracle_rows_timing(A, B, target_s=12.0, max_rows=M)
+        cpu = {"value": 2.0 * rows * N * K / t / 1e12, "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} product ({t:.1f} s, double "
+                         f"accumulation, {threads} threads)"}
+
+    if args.suite and rank == 0:
+        run_suite(g, torch, np, peaks)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "plan": plan,
+                       "l2": "inputs exceed L2 (A+B = 256 MiB > 129 MB); no flush",
+                       "parallelism": "replicas" if world > 1 else "single-gpu"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks,
+            "pct_of_peak": 100.0 * achieved / peaks["bf16_tflops"],
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_suite(g, torch, np, peaks):
+    """Every workload configuration, timed (not part of the JSON line)."""
+    from dense_gemm_tensor_tcgen05_gb300 import inputs
+    cfgs = [("f16", "uniform", 1024, 1024, 1024, 1.0), ("f32", "uniform", 1024, 1024, 1024, 1.0),
+            ("f32", "uniform", 4096, 4096, 4096, 1.0), ("f16", "normal", 2048, 2048, 2048, 1.0),
+            ("bf16", "normal", 8192, 8192, 8192, 1 / math.sqrt(8192)),
+            ("f16", "uniform", 4000, 3000, 1000, 1.0), ("f16", "uniform", 16384, 128, 4096, 1.0),
+            ("f16", "uniform", 8, 8192, 8192, 1.0)]
+    fns = {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32}
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    out = []
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for dt, dist, m, n, k, sigma in cfgs:
+        A = inputs.make(dist, dt, m, k, 1, 0, sigma)
+        B = inputs.make(dist, dt, k, n, 1, 1, sigma)
+        if dt == "f32":
+            Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        else:
+            Ad = torch.from_numpy(A.view(np.int16)).view(tdt[dt]).cuda()
+            Bd = torch.from_numpy(B.view(np.int16)).view(tdt[dt]).cuda()
+        Cd = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        call = lambda: fns[dt](Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), m, n, k, k, n, n, sh)
+        plan = g.gemm_plan_describe({"f16": 0, "bf16": 1, "f32": 2}[dt], Ad.data_ptr(),
+                                    Bd.data_ptr(), Cd.data_ptr(), m, n, k, k, n, n)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        # warm: back to back, at least 100 ms
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        iters = 20
+        while True:
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(iters):
+                    call()
+                e1.record(stream)
+            stream.synchronize()
+            ms = e0.elapsed_time(e1)
+            if ms >= 100 or iters >= 20000:
+                break
+            iters = int(iters * max(2.0, 110.0 / max(ms, 1e-3)))
+        warm_ms = ms / iters
+        # cold: L2 flushed (256 MiB write) before each timed launch
+        cold = []
+        for _ in range(10):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                e0.record(stream)
+                call()
+                e1.record(stream)
+            stream.synchronize()
+            cold.append(e0.elapsed_time(e1))
+        cold_ms = statistics.median(cold)
+        g.gemm_device_error(sh)
+        flop = 2.0 * m * n * k
+        byts = (m * k + k * n) * (4 if dt == "f32" else 2) + m * n * 4
+        out.append({"dtype": dt, "M": m, "N": n, "K": k, "plan": plan,
+                    "warm_ms": warm_ms, "cold_ms": cold_ms,
+                    "tflops_warm": flop / warm_ms / 1e9, "tflops_cold": flop / cold_ms / 1e9,
+                    "gbs_warm": byts / warm_ms / 1e6, "gbs_cold": byts / cold_ms / 1e6,
+                    "frac_tc_peak_warm": flop / warm_ms / 1e9 / peaks["bf16_tflops"]})
+        del Ad, Bd, Cd
+        torch.cuda.empty_cache()
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    with open(os.path.join(ROOT, "gpurun_out", "bench_suite.json"), "w") as f:
+        json.dump(out, f, indent=1)
+    for r in out:
+        sys.stderr.write(json.dumps(r) + "\n")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--suite", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        return run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,255 @@
-"""GB300-native dense GEMM (placeholder; binding follows)."""
+"""GB300-native dense GEMM: Python binding of libgb300gemm.so.
+
+The library computes row-major C = A x B on one GB300 (sm_103a):
+
+  * ``gemm_f16f32`` / ``gemm_bf16f32``: FP16 / BF16 inputs, FP32 accumulate
+    and output, on the tensor cores (TMA + tcgen05.mma, accumulators in tensor
+    memory);
+  * ``sgemm_f32``: FP32 in and out on the CUDA cores.
+
+The functions here carry the C ABI's names and arguments (device pointers as
+ints, sizes, leading dimensions, a stream handle) and only marshal them:
+every step of the product runs in the library's CUDA kernels.  ``matmul`` is
+a convenience wrapper for torch tensors (device memory and streams come from
+torch; nothing else does).  There is no CPU fallback: when the library is
+missing or the GPU is not an sm_103 part, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
+    "gemm_plan_describe", "gemm_device_error", "gemm_release_workspace", "gemm_version",
+    "gemm_launch_count", "matmul", "plan", "GemmOptions", "STATUS", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libgb300gemm.so")
+
+STATUS = {
+    0: "GEMM_OK",
+    1: "GEMM_ERR_INVALID_VALUE",
+    2: "GEMM_ERR_OVERLAP",
+    3: "GEMM_ERR_UNSUPPORTED_DEVICE",
+    4: "GEMM_ERR_LAUNCH",
+    5: "GEMM_ERR_DEVICE_TIMEOUT",
+    6: "GEMM_ERR_CUDA",
+    7: "GEMM_ERR_OUT_OF_MEMORY",
+}
+
+# Every function include/gb300gemm.h declares.
+EXPORTED_SYMBOLS = (
+    "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex", "gemm_plan_describe",
+    "gemm_device_error", "gemm_release_workspace", "gemm_status_string",
+    "gemm_last_cuda_error", "gemm_version", "gemm_launch_count",
+)
+
+
+class GemmError(RuntimeError):
+    """A non-OK gemm_status_t."""
+
+    def __init__(self, status: int, detail: str = ""):
+        self.status = status
+        self.name = STATUS.get(status, f"status {status}")
+        super().__init__(f"{self.name}{': ' + detail if detail else ''}")
+
+
+class GemmOptions(ctypes.Structure):
+    """gemm_options_t (see include/gb300gemm.h)."""
+    _fields_ = [("dtype", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
+                ("generic", ctypes.c_int32), ("group_m", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgb300gemm.so (built in-tree by ``build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(
+                    f"{library_path} is missing: build it with "
+                    "`python -m dense_gemm_tensor_tcgen05_gb300.build` (needs nvcc)")
+            L = ctypes.CDLL(library_path)
+            vp, i64 = ctypes.c_void_p, ctypes.c_int64
+            sig = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+            for name in ("gemm_f16f32", "gemm_bf16f32", "sgemm_f32"):
+                f = getattr(L, name)
+                f.argtypes = sig
+                f.restype = ctypes.c_int
+            L.gemm_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                  ctypes.POINTER(GemmOptions), vp]
+            L.gemm_ex.restype = ctypes.c_int
+            L.gemm_plan_describe.argtypes = [ctypes.c_int32, vp, vp, vp, i64, i64, i64, i64, i64,
+                                             i64, ctypes.POINTER(GemmOptions), ctypes.c_char_p, i64]
+            L.gemm_plan_describe.restype = ctypes.c_int
+            L.gemm_device_error.argtypes = [vp]
+            L.gemm_device_error.restype = ctypes.c_int
+            L.gemm_release_workspace.argtypes = []
+            L.gemm_release_workspace.restype = ctypes.c_int
+            L.gemm_status_string.argtypes = [ctypes.c_int]
+            L.gemm_status_string.restype = ctypes.c_char_p
+            L.gemm_last_cuda_error.argtypes = []
+            L.gemm_last_cuda_error.restype = ctypes.c_char_p
+            L.gemm_version.argtypes = []
+            L.gemm_version.restype = ctypes.c_int32
+            L.gemm_launch_count.argtypes = []
+            L.gemm_launch_count.restype = ctypes.c_int64
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        detail = lib().gemm_last_cuda_error().decode(errors="replace")
+        raise GemmError(status, detail)
+
+
+# ---- the C ABI, one Python function per entry point (marshalling only) ----
+
+def gemm_f16f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                stream: int = 0) -> None:
+    _check(lib().gemm_f16f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None))
+
+
+def gemm_bf16f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                 stream: int = 0) -> None:
+    _check(lib().gemm_bf16f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None))
+
+
+def sgemm_f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+              stream: int = 0) -> None:
+    _check(lib().sgemm_f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None))
+
+
+def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0) -> GemmOptions:
+    o = GemmOptions()
+    o.dtype, o.tile_n, o.split_k, o.swap_ab, o.generic, o.group_m = (
+        dtype, tile_n, split_k, swap_ab, generic, group_m)
+    return o
+
+
+def gemm_ex(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+            dtype: int, stream: int = 0, **opts) -> None:
+    o = _options(dtype, **opts)
+    _check(lib().gemm_ex(A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o), stream or None))
+
+
+def gemm_plan_describe(dtype: int, A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
+                       ldb: int, ldc: int, **opts) -> str:
+    o = _options(dtype, **opts)
+    buf = ctypes.create_string_buffer(512)
+    _check(lib().gemm_plan_describe(dtype, A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o),
+                                    buf, len(buf)))
+    return buf.value.decode()
+
+
+def gemm_device_error(stream: int = 0) -> None:
+    _check(lib().gemm_device_error(stream or None))
+
+
+def gemm_release_workspace() -> None:
+    _check(lib().gemm_release_workspace())
+
+
+def gemm_version() -> int:
+    return int(lib().gemm_version())
+
+
+def gemm_launch_count() -> int:
+    return int(lib().gemm_launch_count())
+
+
+# ---- torch convenience -------------------------------------------------------
+
+_DTYPE_CODE = {"float16": 0, "bfloat16": 1, "float32": 2}
+
+
+def _code(t) -> int:
+    name = str(t.dtype).replace("torch.", "")
+    if name not in _DTYPE_CODE:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DTYPE_CODE[name]
+
+
+def _row_major_ld(t, name: str) -> int:
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.stride(1) != 1 and t.size(1) > 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    return max(t.stride(0), t.size(1)) if t.size(0) > 1 else max(t.size(1), 1)
+
+
+def matmul(A, B, out=None, stream=None, **opts):
+    """C = A @ B for 2-D CUDA tensors (row-major, any row stride).
+
+    A and B: both float16, both bfloat16 or both float32; C is float32.
+    Inputs on the CPU are copied to the current device, the product runs
+    there, and the result is copied back into a CPU tensor (the copies are
+    issued on the same stream).  ``opts`` are gemm_options_t fields
+    (tile_n, split_k, swap_ab, generic, group_m) and route through gemm_ex.
+    """
+    import torch
+
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    code = _code(A)
+    host = not A.is_cuda
+    if host != (not B.is_cuda):
+        raise ValueError("A and B must both be on the GPU or both on the host")
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if host:
+        with torch.cuda.stream(st):
+            Ad = A.to("cuda", non_blocking=True)
+            Bd = B.to("cuda", non_blocking=True)
+    else:
+        Ad, Bd = A, B
+    M, K = Ad.shape
+    K2, N = Bd.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None or host:
+        with torch.cuda.stream(st):
+            Cd = torch.empty((M, N), dtype=torch.float32, device=Ad.device)
+    else:
+        Cd = out
+        if Cd.dtype != torch.float32 or tuple(Cd.shape) != (M, N):
+            raise ValueError("out must be float32 of shape (M, N)")
+    lda, ldb, ldc = _row_major_ld(Ad, "A"), _row_major_ld(Bd, "B"), _row_major_ld(Cd, "C")
+    args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, lda, ldb, ldc)
+    sh = st.cuda_stream
+    if opts:
+        gemm_ex(*args, dtype=code, stream=sh, **opts)
+    elif code == 0:
+        gemm_f16f32(*args, stream=sh)
+    elif code == 1:
+        gemm_bf16f32(*args, stream=sh)
+    else:
+        sgemm_f32(*args, stream=sh)
+    if host:
+        res = out if out is not None else torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+        with torch.cuda.stream(st):
+            res.copy_(Cd, non_blocking=True)
+        st.synchronize()
+        return res
+    return Cd
+
+
+def plan(A, B, out=None, **opts) -> str:
+    """The plan text gemm_plan_describe gives for torch tensors A @ B."""
+    code = _code(A)
+    M, K = A.shape
+    _, N = B.shape
+    # Only C's alignment is read; without `out`, describe a 256-byte aligned C.
+    cptr = out.data_ptr() if out is not None else 256
+    ldc = _row_major_ld(out, "C") if out is not None else N
+    return gemm_plan_describe(code, A.data_ptr(), B.data_ptr(), cptr, M, N, K,
+                              _row_major_ld(A, "A"), _row_major_ld(B, "B"), ldc, **opts)

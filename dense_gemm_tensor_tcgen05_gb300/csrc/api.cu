@@ -1,0 +1,496 @@
+// api.cu -- the C ABI declared in include/gb300gemm.h: argument checks,
+// planning, the split-K workspace and kernel launches.
+//
+// The operation and its conventions (row-major, leading dimension = row
+// stride in elements, C overwritten) are those of the header; see there for
+// the page passages they follow.
+
+#include <climits>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/gb300gemm.h"
+#include "internal.h"
+
+using namespace gb300;
+
+namespace {
+
+thread_local char t_last_error[256] = "";
+thread_local int64_t t_launches = 0;
+
+void note_cuda_error(cudaError_t e, const char* where) {
+    snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+             cudaGetErrorString(e));
+}
+
+// ---- device facts --------------------------------------------------------------
+
+struct DeviceInfo {
+    bool valid = false;
+    int major = 0, minor = 0, sms = 0;
+};
+
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_dev;
+
+gemm_status_t current_device(int* dev, DeviceInfo* info) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaGetDevice");
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[*dev];
+    if (!d.valid) {
+        cudaDeviceProp p;
+        e = cudaGetDeviceProperties(&p, *dev);
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaGetDeviceProperties");
+            return GEMM_ERR_CUDA;
+        }
+        d.major = p.major;
+        d.minor = p.minor;
+        d.sms = p.multiProcessorCount;
+        d.valid = true;
+    }
+    *info = d;
+    if (d.major != 10 || d.minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    return GEMM_OK;
+}
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// ---- split-K workspace, one per (device, stream) --------------------------------
+
+struct Workspace {
+    float* ws = nullptr;
+    size_t ws_floats = 0;
+    uint32_t* counters = nullptr;
+    size_t n_counters = 0;
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+gemm_status_t get_workspace(int dev, cudaStream_t stream, size_t floats, size_t counters,
+                            float** ws, uint32_t** cnt) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[{dev, stream}];
+    if (w.ws_floats < floats) {
+        if (w.ws) {
+            cudaStreamSynchronize(stream);   // the old buffer may still be in use on this stream
+            cudaFree(w.ws);
+            w.ws = nullptr;
+            w.ws_floats = 0;
+        }
+        cudaError_t e = cudaMalloc(&w.ws, floats * sizeof(float));
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaMalloc(split-K workspace)");
+            w.ws = nullptr;
+            return GEMM_ERR_OUT_OF_MEMORY;
+        }
+        w.ws_floats = floats;
+    }
+    if (w.n_counters < counters) {
+        if (w.counters) {
+            cudaStreamSynchronize(stream);
+            cudaFree(w.counters);
+            w.counters = nullptr;
+            w.n_counters = 0;
+        }
+        cudaError_t e = cudaMalloc(&w.counters, counters * sizeof(uint32_t));
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaMalloc(split-K counters)");
+            w.counters = nullptr;
+            return GEMM_ERR_OUT_OF_MEMORY;
+        }
+        // Counters start at zero and every launch leaves them at zero.
+        e = cudaMemsetAsync(w.counters, 0, counters * sizeof(uint32_t), stream);
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaMemsetAsync(split-K counters)");
+            return GEMM_ERR_CUDA;
+        }
+        w.n_counters = counters;
+    }
+    *ws = w.ws;
+    *cnt = w.counters;
+    return GEMM_OK;
+}
+
+// ---- argument checks -------------------------------------------------------------
+
+bool spans_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+    return a0 < b1 && b0 < a1;
+}
+
+gemm_status_t check_args(const void* A, const void* B, const float* C, int64_t M, int64_t N,
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int esize) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
+    if (lda < K || ldb < N || ldc < N) return GEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_INVALID_VALUE;
+    if (K > 0 && (!A || !B)) return GEMM_ERR_INVALID_VALUE;
+    // keep every byte offset well inside int64
+    const int64_t lim = INT64_MAX / 16;
+    if ((M > 1 && ldc > lim / (M - 1)) || (M > 1 && lda > lim / (M - 1)) ||
+        (K > 1 && ldb > lim / (K - 1)))
+        return GEMM_ERR_INVALID_VALUE;
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(C);
+    const uintptr_t c1 = c0 + static_cast<uintptr_t>((M - 1) * ldc + N) * 4;
+    if (K > 0) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(A);
+        const uintptr_t a1 = a0 + static_cast<uintptr_t>((M - 1) * lda + K) * esize;
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(B);
+        const uintptr_t b1 = b0 + static_cast<uintptr_t>((K - 1) * ldb + N) * esize;
+        if (spans_overlap(c0, c1, a0, a1) || spans_overlap(c0, c1, b0, b1)) return GEMM_ERR_OVERLAP;
+    }
+    return GEMM_OK;
+}
+
+// ---- planning ----------------------------------------------------------------------
+
+enum class Kind { Nothing, ZeroFill, Tc, Generic, Sgemm };
+
+struct Plan {
+    Kind kind = Kind::Nothing;
+    TcLaunch tc{};
+    int sg_bm = 0, sg_bn = 0;
+    int64_t units = 0;
+    size_t ws_floats = 0, n_counters = 0;
+};
+
+gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64_t M, int64_t N,
+                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        const gemm_options_t& o, int sms, Plan* plan) {
+    Plan p;
+    if (M == 0 || N == 0) {
+        *plan = p;
+        return GEMM_OK;
+    }
+    if (K == 0) {
+        p.kind = Kind::ZeroFill;
+        *plan = p;
+        return GEMM_OK;
+    }
+    if (dtype == 2) {
+        const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+                               reinterpret_cast<uintptr_t>(C)) & 15) == 0 &&
+                             (lda & 3) == 0 && (ldb & 3) == 0 && (ldc & 3) == 0;
+        if (o.generic || !aligned) {
+            p.kind = Kind::Generic;
+        } else {
+            p.kind = Kind::Sgemm;
+            const int64_t t128 = ceil_div(M, 128) * ceil_div(N, 128);
+            const int64_t t64 = ceil_div(M, 128) * ceil_div(N, 64);
+            if (o.tile_n == 128 || (o.tile_n == 0 && t128 >= sms)) {
+                p.sg_bm = 128; p.sg_bn = 128;
+            } else if (o.tile_n == 64 || (o.tile_n == 0 && t64 >= sms)) {
+                p.sg_bm = 128; p.sg_bn = 64;
+            } else if (o.tile_n == 0 || o.tile_n == 32) {
+                p.sg_bm = 64; p.sg_bn = 64;
+            } else {
+                return GEMM_ERR_INVALID_VALUE;
+            }
+        }
+        *plan = p;
+        return GEMM_OK;
+    }
+
+    // 16-bit inputs: TMA needs 16-byte aligned bases and row strides.
+    const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0 &&
+                        (lda & 7) == 0 && (ldb & 7) == 0;
+    if (o.generic || !tma_ok) {
+        p.kind = Kind::Generic;
+        *plan = p;
+        return GEMM_OK;
+    }
+    TcLaunch& L = p.tc;
+    L.A = A; L.B = B; L.C = C;
+    L.M = M; L.N = N; L.K = K; L.lda = lda; L.ldb = ldb; L.ldc = ldc;
+    L.fmt = dtype;
+    L.swap = (o.swap_ab < 0) ? ((M <= 64 && N > M) ? 1 : 0) : (o.swap_ab ? 1 : 0);
+
+    const int64_t pe = L.swap ? N : M;     // extent along the MMA M side
+    const int64_t qe = L.swap ? M : N;     // extent along the MMA N side
+    if (o.tile_n) {
+        if (!tc_config_supported(o.tile_n, L.swap)) return GEMM_ERR_INVALID_VALUE;
+        L.bn = o.tile_n;
+    } else if (L.swap) {
+        L.bn = qe <= 16 ? 16 : qe <= 32 ? 32 : 64;
+    } else if (qe <= 64) {
+        L.bn = 64;
+    } else {
+        // fewest estimated tile-time units: waves x (tile width + fixed cost)
+        const int cand[3] = {256, 128, 64};
+        int64_t best = INT64_MAX;
+        for (int bn : cand) {
+            if (bn > 128 && qe <= 128) continue;
+            const int64_t tiles = ceil_div(pe, kTcBM) * ceil_div(qe, bn);
+            const int64_t cost = ceil_div(tiles, sms) * (bn + 64);
+            if (cost < best) {
+                best = cost;
+                L.bn = bn;
+            }
+        }
+    }
+    const int64_t tiles_p = ceil_div(pe, kTcBM);
+    const int64_t tiles = tiles_p * ceil_div(qe, L.bn);
+    const int64_t kb_total = ceil_div(K, kTcBK);
+
+    int64_t splits = 1;
+    if (o.split_k > 0) {
+        if (o.split_k > 64) return GEMM_ERR_INVALID_VALUE;
+        splits = o.split_k;
+    } else if (tiles * 2 <= sms && kb_total >= 4) {
+        // few tiles: split K so that more SMs stream operands.  Minimise
+        // waves x (1/S + a fixed cost per unit).
+        double best = 1e30;
+        const int64_t smax = std::min<int64_t>(16, kb_total / 2);
+        for (int64_t s = 1; s <= smax; ++s) {
+            const double cost = static_cast<double>(ceil_div(tiles * s, sms)) * (1.0 / s + 0.05);
+            if (cost < best - 1e-12) {
+                best = cost;
+                splits = s;
+            }
+        }
+    }
+    if (splits > kb_total) splits = kb_total;
+    const int64_t kb_per = ceil_div(kb_total, splits);
+    splits = ceil_div(kb_total, kb_per);   // no empty slices
+    L.splits = static_cast<int>(splits);
+
+    int64_t group = o.group_m > 0 ? o.group_m : 16;
+    if (group > tiles_p) group = tiles_p;
+    L.group = static_cast<int>(group);
+
+    p.units = tiles * splits;
+    L.grid = static_cast<int>(std::min<int64_t>(p.units, sms));
+    if (splits > 1) {
+        p.ws_floats = static_cast<size_t>(tiles * splits * kTcBM * L.bn);
+        p.n_counters = static_cast<size_t>(tiles * 4);
+    }
+    p.kind = Kind::Tc;
+    *plan = p;
+    return GEMM_OK;
+}
+
+void describe(const Plan& p, int dtype, char* buf, int64_t size) {
+    if (!buf || size <= 0) return;
+    const int n = static_cast<int>(size > INT32_MAX ? INT32_MAX : size);
+    switch (p.kind) {
+        case Kind::Nothing: snprintf(buf, n, "nothing (empty output)"); break;
+        case Kind::ZeroFill: snprintf(buf, n, "zero-fill (K == 0)"); break;
+        case Kind::Generic: snprintf(buf, n, "generic cuda-core dtype=%d tile=64x64", dtype); break;
+        case Kind::Sgemm: snprintf(buf, n, "sgemm tile=%dx%dx8", p.sg_bm, p.sg_bn); break;
+        case Kind::Tc:
+            snprintf(buf, n,
+                     "tcgen05 fmt=%s tile=128x%d swap=%d split_k=%d group=%d units=%lld grid=%d",
+                     p.tc.fmt ? "bf16" : "f16", p.tc.bn, p.tc.swap, p.tc.splits, p.tc.group,
+                     static_cast<long long>(p.units), p.tc.grid);
+            break;
+    }
+}
+
+gemm_status_t launch_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) {
+        ++t_launches;
+        return GEMM_OK;
+    }
+    note_cuda_error(e, what);
+    cudaGetLastError();   // clear a non-sticky launch error
+    return GEMM_ERR_LAUNCH;
+}
+
+gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, int64_t N,
+                  int64_t K, int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t& o,
+                  cudaStream_t stream) {
+    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
+    const int esize = dtype == 2 ? 4 : 2;
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    int dev;
+    DeviceInfo info;
+    st = current_device(&dev, &info);
+    if (st != GEMM_OK) return st;
+    Plan p;
+    st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, o, info.sms, &p);
+    if (st != GEMM_OK) return st;
+    switch (p.kind) {
+        case Kind::Nothing: return GEMM_OK;
+        case Kind::ZeroFill: return launch_status(fill_zero_launch(C, M, N, ldc, stream), "fill_zero");
+        case Kind::Generic:
+            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, stream),
+                                 "generic_gemm");
+        case Kind::Sgemm:
+            return launch_status(sgemm_launch(p.sg_bm, p.sg_bn, static_cast<const float*>(A),
+                                              static_cast<const float*>(B), C, M, N, K, lda, ldb,
+                                              ldc, stream),
+                                 "sgemm");
+        case Kind::Tc: {
+            EncodeTiledFn enc = encode_fn();
+            if (!enc) {
+                snprintf(t_last_error, sizeof(t_last_error),
+                         "cuTensorMapEncodeTiled entry point unavailable");
+                return GEMM_ERR_CUDA;
+            }
+            if (p.tc.splits > 1) {
+                st = get_workspace(dev, stream, p.ws_floats, p.n_counters, &p.tc.ws, &p.tc.counters);
+                if (st != GEMM_OK) return st;
+            }
+            return launch_status(tc_gemm_launch(p.tc, enc, stream), "tc_gemm");
+        }
+    }
+    return GEMM_ERR_INVALID_VALUE;
+}
+
+gemm_options_t default_options(int dtype) {
+    gemm_options_t o;
+    memset(&o, 0, sizeof(o));
+    o.dtype = dtype;
+    o.swap_ab = -1;
+    return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_f16f32(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc, gemm_stream_t stream) {
+    return run(0, A, B, C, M, N, K, lda, ldb, ldc, default_options(0),
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_bf16f32(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldc, gemm_stream_t stream) {
+    return run(1, A, B, C, M, N, K, lda, ldb, ldc, default_options(1),
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t sgemm_f32(const float* A, const float* B, float* C, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc, gemm_stream_t stream) {
+    return run(2, A, B, C, M, N, K, lda, ldb, ldc, default_options(2),
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_ex(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t* options,
+                      gemm_stream_t stream) {
+    if (!options) return GEMM_ERR_INVALID_VALUE;
+    return run(options->dtype, A, B, C, M, N, K, lda, ldb, ldc, *options,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, const float* C,
+                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t ldc, const gemm_options_t* options, char* buf,
+                                 int64_t size) {
+    if (buf && size > 0) buf[0] = '\0';
+    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2);
+    if (st != GEMM_OK) return st;
+    int dev;
+    DeviceInfo info;
+    st = current_device(&dev, &info);
+    if (st != GEMM_OK) return st;
+    gemm_options_t o = options ? *options : default_options(dtype);
+    Plan p;
+    st = make_plan(dtype, A, B, const_cast<float*>(C), M, N, K, lda, ldb, ldc, o, info.sms, &p);
+    if (st == GEMM_OK) describe(p, dtype, buf, size);
+    return st;
+}
+
+gemm_status_t gemm_device_error(gemm_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaStreamSynchronize");
+        return GEMM_ERR_CUDA;
+    }
+    uint32_t* word = nullptr;
+    e = tc_error_word(&word);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaGetSymbolAddress");
+        return GEMM_ERR_CUDA;
+    }
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaMemcpy(error word)");
+        return GEMM_ERR_CUDA;
+    }
+    if (v) {
+        e = cudaMemset(word, 0, sizeof(uint32_t));
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaMemset(error word)");
+            return GEMM_ERR_CUDA;
+        }
+        snprintf(t_last_error, sizeof(t_last_error), "device pipeline wait gave up (bits 0x%x)", v);
+        return GEMM_ERR_DEVICE_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_release_workspace(void) {
+    int dev;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaGetDevice");
+        return GEMM_ERR_CUDA;
+    }
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaDeviceSynchronize");
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto it = g_ws.begin(); it != g_ws.end();) {
+        if (it->first.first == dev) {
+            cudaFree(it->second.ws);
+            cudaFree(it->second.counters);
+            it = g_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE: invalid argument";
+        case GEMM_ERR_OVERLAP: return "GEMM_ERR_OVERLAP: C overlaps A or B";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a device pipeline wait gave up";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime call failed";
+        case GEMM_ERR_OUT_OF_MEMORY: return "GEMM_ERR_OUT_OF_MEMORY: workspace allocation failed";
+    }
+    return "unknown gemm_status_t";
+}
+
+const char* gemm_last_cuda_error(void) { return t_last_error; }
+
+int32_t gemm_version(void) { return 100; }
+
+int64_t gemm_launch_count(void) { return t_launches; }
+
+}  // extern "C"

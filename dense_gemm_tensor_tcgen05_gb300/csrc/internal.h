@@ -1,0 +1,59 @@
+// internal.h -- declarations shared by the library's translation units
+// (host side only; not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300 {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// One tensor-core GEMM launch, fully planned.
+struct TcLaunch {
+    const void* A;
+    const void* B;
+    float* C;
+    int64_t M, N, K, lda, ldb, ldc;
+    int fmt;        // 0 = FP16, 1 = BF16
+    int bn;         // tile width along the MMA N side
+    int swap;       // 1: MMA M side runs along N of C (C^T = B^T A^T)
+    int splits;     // K slices
+    int group;      // raster group height in tiles along the MMA M side
+    int grid;       // CTAs (persistent); <= units
+    float* ws;          // split-K partial tiles (splits * tiles * 128 * bn floats), or null
+    uint32_t* counters; // split-K arrival counters (tiles * 4), zero between launches, or null
+};
+
+// Tile geometry helpers used by the planner and the launcher.
+constexpr int kTcBM = 128;  // rows along the MMA M side (= tensor-memory lanes)
+constexpr int kTcBK = 64;   // k per pipeline stage (64 16-bit elements = 128 bytes)
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Which (bn, swap) kernels exist.
+bool tc_config_supported(int bn, int swap);
+
+// Launch the tensor-core kernel.  Returns the first CUDA error (tensor-map
+// encoding failures are reported as cudaErrorInvalidValue).
+cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t stream);
+
+// Device address of this device's error word (cudaGetSymbolAddress on the
+// tensor-core translation unit's __device__ variable).
+cudaError_t tc_error_word(uint32_t** ptr);
+
+// CUDA-core kernels.
+bool sgemm_tile_supported(int bm, int bn);
+cudaError_t sgemm_launch(int bm, int bn, const float* A, const float* B, float* C, int64_t M,
+                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                         cudaStream_t stream);
+cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           cudaStream_t stream);
+cudaError_t fill_zero_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream);
+
+}  // namespace gb300

@@ -1,0 +1,334 @@
+// sgemm.cu -- CUDA-core kernels: the FP32 SGEMM, a guarded generic GEMM for
+// inputs the vectorised or TMA paths cannot take, and the K == 0 fill.
+//
+// SGEMM design (the register-tiling ladder of "matmul_registers.cu" carried
+// to its last step, re-derived for sm_103a):
+//   * a CTA computes a BM x BN tile of C; each thread owns an 8 x 8 register
+//     micro-tile split into four 4 x 4 quadrants (rows ty*4.. and BM/2+ty*4..,
+//     columns tx*4.. and BN/2+tx*4..), so every shared-memory fragment read is
+//     one float4 and a warp's reads hit distinct banks;
+//   * per K step of BK, A (BM x BK) and B (BK x BN) slices come in with float4
+//     global loads; A is stored transposed (k-major rows of BM floats, padded
+//     by 4 so the transposing stores are conflict-free), which makes the
+//     inner loop read four consecutive rows of A with one instruction;
+//   * two shared-memory buffers: the next slice is loaded into registers
+//     while the current one is multiplied, then stored to the other buffer,
+//     with one barrier per K step;
+//   * 64 FFMA per 4 float4 shared loads in the inner loop.
+// Edges: each CTA decides once whether its tile lies wholly inside C; only
+// boundary tiles use guarded loads and masked stores, and only the last,
+// partial K step of any tile uses guarded loads.  Misaligned pointers or
+// leading dimensions go to the generic kernel instead.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdio>
+
+#include "internal.h"
+
+namespace gb300 {
+
+// ---------------------------------------------------------------- SGEMM --
+
+template <int BM, int BN, int BK>
+struct SgemmCfg {
+    static constexpr int kTx = BN / 8;             // threads along N
+    static constexpr int kTy = BM / 8;             // threads along M
+    static constexpr int kThreads = kTx * kTy;
+    static constexpr int kAStride = BM + 4;        // padded row of the transposed A slice
+    static constexpr int kALoads = BM * BK / 4;    // float4 per A slice
+    static constexpr int kBLoads = BK * BN / 4;    // float4 per B slice
+    static constexpr int kAPer = (kALoads + kThreads - 1) / kThreads;
+    static constexpr int kBPer = (kBLoads + kThreads - 1) / kThreads;
+    static_assert(BM % 8 == 0 && BN % 8 == 0 && BK % 4 == 0, "tile shape");
+    static_assert(kThreads % 32 == 0 && kThreads <= 1024, "whole warps");
+    static_assert(kALoads % kThreads == 0 && kBLoads % kThreads == 0, "even load split");
+    static_assert(2 * (BK * kAStride + BK * BN) * 4 <= 48 * 1024, "static shared memory");
+};
+
+template <int BM, int BN, int BK, bool EDGE>
+__device__ __forceinline__ void sgemm_load(const float* __restrict__ A, const float* __restrict__ B,
+                                           int M, int N, int K, int64_t lda, int64_t ldb,
+                                           int m0, int n0, int k0, bool guard_k,
+                                           float4 (&ra)[SgemmCfg<BM, BN, BK>::kAPer],
+                                           float4 (&rb)[SgemmCfg<BM, BN, BK>::kBPer]) {
+    using Cfg = SgemmCfg<BM, BN, BK>;
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int l = 0; l < Cfg::kAPer; ++l) {
+        const int idx = tid + l * Cfg::kThreads;
+        const int r = idx / (BK / 4);
+        const int kq = (idx % (BK / 4)) * 4;
+        const int gm = m0 + r, gk = k0 + kq;
+        const float* src = A + static_cast<int64_t>(gm) * lda + gk;
+        if (!EDGE && !guard_k) {
+            ra[l] = __ldg(reinterpret_cast<const float4*>(src));
+        } else if (gm < M && gk + 3 < K) {
+            ra[l] = __ldg(reinterpret_cast<const float4*>(src));
+        } else {
+            float t[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) t[i] = (gm < M && gk + i < K) ? __ldg(src + i) : 0.0f;
+            ra[l] = make_float4(t[0], t[1], t[2], t[3]);
+        }
+    }
+#pragma unroll
+    for (int l = 0; l < Cfg::kBPer; ++l) {
+        const int idx = tid + l * Cfg::kThreads;
+        const int kr = idx / (BN / 4);
+        const int nq = (idx % (BN / 4)) * 4;
+        const int gk = k0 + kr, gn = n0 + nq;
+        const float* src = B + static_cast<int64_t>(gk) * ldb + gn;
+        if (!EDGE && !guard_k) {
+            rb[l] = __ldg(reinterpret_cast<const float4*>(src));
+        } else if (gk < K && gn + 3 < N) {
+            rb[l] = __ldg(reinterpret_cast<const float4*>(src));
+        } else {
+            float t[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) t[i] = (gk < K && gn + i < N) ? __ldg(src + i) : 0.0f;
+            rb[l] = make_float4(t[0], t[1], t[2], t[3]);
+        }
+    }
+}
+
+template <int BM, int BN, int BK>
+__device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs,
+                                                 const float4 (&ra)[SgemmCfg<BM, BN, BK>::kAPer],
+                                                 const float4 (&rb)[SgemmCfg<BM, BN, BK>::kBPer]) {
+    using Cfg = SgemmCfg<BM, BN, BK>;
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int l = 0; l < Cfg::kAPer; ++l) {
+        const int idx = tid + l * Cfg::kThreads;
+        const int r = idx / (BK / 4);
+        const int kq = (idx % (BK / 4)) * 4;
+        As[(kq + 0) * Cfg::kAStride + r] = ra[l].x;
+        As[(kq + 1) * Cfg::kAStride + r] = ra[l].y;
+        As[(kq + 2) * Cfg::kAStride + r] = ra[l].z;
+        As[(kq + 3) * Cfg::kAStride + r] = ra[l].w;
+    }
+#pragma unroll
+    for (int l = 0; l < Cfg::kBPer; ++l) {
+        const int idx = tid + l * Cfg::kThreads;
+        const int kr = idx / (BN / 4);
+        const int nq = (idx % (BN / 4)) * 4;
+        *reinterpret_cast<float4*>(Bs + kr * BN + nq) = rb[l];
+    }
+}
+
+template <int BM, int BN, int BK, bool EDGE>
+__device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B,
+                                           float* __restrict__ C, int M, int N, int K,
+                                           int64_t lda, int64_t ldb, int64_t ldc, int m0, int n0,
+                                           float* As0, float* Bs0) {
+    using Cfg = SgemmCfg<BM, BN, BK>;
+    const int tx = threadIdx.x % Cfg::kTx;
+    const int ty = threadIdx.x / Cfg::kTx;
+    const int k_tiles = (K + BK - 1) / BK;
+    const int k_full = K / BK;   // slices with no K tail
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    float4 ra[Cfg::kAPer], rb[Cfg::kBPer];
+    sgemm_load<BM, BN, BK, EDGE>(A, B, M, N, K, lda, ldb, m0, n0, 0, 0 >= k_full, ra, rb);
+    sgemm_store_smem<BM, BN, BK>(As0, Bs0, ra, rb);
+    __syncthreads();
+
+    for (int kt = 0; kt < k_tiles; ++kt) {
+        float* As = As0 + (kt & 1) * (BK * Cfg::kAStride);
+        float* Bs = Bs0 + (kt & 1) * (BK * BN);
+        const bool more = kt + 1 < k_tiles;
+        if (more)
+            sgemm_load<BM, BN, BK, EDGE>(A, B, M, N, K, lda, ldb, m0, n0, (kt + 1) * BK,
+                                         kt + 1 >= k_full, ra, rb);
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + ty * 4);
+            const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + BM / 2 + ty * 4);
+            const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * BN + tx * 4);
+            const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * BN + BN / 2 + tx * 4);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (more) {
+            float* An = As0 + ((kt + 1) & 1) * (BK * Cfg::kAStride);
+            float* Bn = Bs0 + ((kt + 1) & 1) * (BK * BN);
+            sgemm_store_smem<BM, BN, BK>(An, Bn, ra, rb);
+        }
+        __syncthreads();
+    }
+
+    // store: quadrant (qi, qj) rows m0 + qi*BM/2 + ty*4 + i, columns n0 + qj*BN/2 + tx*4 + j
+#pragma unroll
+    for (int qi = 0; qi < 2; ++qi) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gm = m0 + qi * (BM / 2) + ty * 4 + i;
+            if (EDGE && gm >= M) continue;
+            float* crow = C + static_cast<int64_t>(gm) * ldc;
+#pragma unroll
+            for (int qj = 0; qj < 2; ++qj) {
+                const int gn = n0 + qj * (BN / 2) + tx * 4;
+                const float* v = &acc[qi * 4 + i][qj * 4];
+                if (!EDGE) {
+                    *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (gn + j < N) crow[gn + j] = v[j];
+                }
+            }
+        }
+    }
+}
+
+template <int BM, int BN, int BK>
+__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK>::kThreads)
+sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
+             int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc) {
+    using Cfg = SgemmCfg<BM, BN, BK>;
+    __shared__ __align__(16) float As[2 * BK * Cfg::kAStride];
+    __shared__ __align__(16) float Bs[2 * BK * BN];
+    const int m0 = blockIdx.y * BM;
+    const int n0 = blockIdx.x * BN;
+    if (m0 + BM <= M && n0 + BN <= N)
+        sgemm_tile<BM, BN, BK, false>(A, B, C, M, N, K, lda, ldb, ldc, m0, n0, As, Bs);
+    else
+        sgemm_tile<BM, BN, BK, true>(A, B, C, M, N, K, lda, ldb, ldc, m0, n0, As, Bs);
+}
+
+template <int BM, int BN, int BK>
+static cudaError_t sgemm_go(const float* A, const float* B, float* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
+    dim3 grid(static_cast<unsigned>(ceil_div(N, BN)), static_cast<unsigned>(ceil_div(M, BM)));
+    sgemm_kernel<BM, BN, BK><<<grid, SgemmCfg<BM, BN, BK>::kThreads, 0, stream>>>(
+        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), lda, ldb, ldc);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- generic --
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 64 x 64 tile per CTA of 256 threads, 4 x 4 outputs per thread, K steps of
+// 16, every access guarded: any alignment, any leading dimension.
+template <typename T>
+__global__ void __launch_bounds__(256)
+generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __restrict__ C,
+                    int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc) {
+    __shared__ float As[16][64 + 1];
+    __shared__ float Bs[16][64 + 1];
+    const int tid = threadIdx.x;
+    const int tx = tid % 16, ty = tid / 16;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        for (int l = tid; l < 64 * 16; l += 256) {
+            const int r = l / 16, c = l % 16;     // A: 64 rows x 16 k
+            const int gm = m0 + r, gk = k0 + c;
+            As[c][r] = (gm < M && gk < K) ? to_f32(A[static_cast<int64_t>(gm) * lda + gk]) : 0.0f;
+            const int kr = l / 64, nc = l % 64;   // B: 16 k x 64 cols
+            const int bk = k0 + kr, bn = n0 + nc;
+            Bs[kr][nc] = (bk < K && bn < N) ? to_f32(B[static_cast<int64_t>(bk) * ldb + bn]) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[k][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[k][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gm = m0 + ty + 16 * i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tx + 16 * j;
+            if (gn < N) C[static_cast<int64_t>(gm) * ldc + gn] = acc[i][j];
+        }
+    }
+}
+
+__global__ void fill_zero_kernel(float* C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / N, c = i - r * N;
+        C[r * ldc + c] = 0.0f;
+    }
+}
+
+// ---------------------------------------------------------------- host --
+
+bool sgemm_tile_supported(int bm, int bn) {
+    return (bm == 128 && bn == 128) || (bm == 128 && bn == 64) || (bm == 64 && bn == 64);
+}
+
+cudaError_t sgemm_launch(int bm, int bn, const float* A, const float* B, float* C, int64_t M,
+                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                         cudaStream_t stream) {
+    if (bm == 128 && bn == 128) return sgemm_go<128, 128, 8>(A, B, C, M, N, K, lda, ldb, ldc, stream);
+    if (bm == 128 && bn == 64) return sgemm_go<128, 64, 8>(A, B, C, M, N, K, lda, ldb, ldc, stream);
+    if (bm == 64 && bn == 64) return sgemm_go<64, 64, 8>(A, B, C, M, N, K, lda, ldb, ldc, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           cudaStream_t stream) {
+    dim3 grid(static_cast<unsigned>(ceil_div(N, 64)), static_cast<unsigned>(ceil_div(M, 64)));
+    const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+    switch (dtype) {
+        case 0:
+            generic_gemm_kernel<__half><<<grid, 256, 0, stream>>>(
+                static_cast<const __half*>(A), static_cast<const __half*>(B), C, m, n, k, lda, ldb, ldc);
+            break;
+        case 1:
+            generic_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), C, m, n,
+                k, lda, ldb, ldc);
+            break;
+        default:
+            generic_gemm_kernel<float><<<grid, 256, 0, stream>>>(
+                static_cast<const float*>(A), static_cast<const float*>(B), C, m, n, k, lda, ldb, ldc);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t fill_zero_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream) {
+    const int64_t total = M * N;
+    int64_t blocks = ceil_div(total, 256);
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    fill_zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc);
+    return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -1,0 +1,501 @@
+// tc_gemm.cu -- persistent, warp-specialised tensor-core GEMM for sm_103a.
+//
+// C (FP32) = A x B with FP16 or BF16 A and B, FP32 accumulation, row-major
+// everything.  The tile decomposition is the one the pages describe for
+// tensor cores -- loop over output tiles, accumulate the tile over K slices,
+// store it once ("Tensor cores and matrix operations", "Complete Algorithm
+// for Large Matrix Multiply") -- mapped onto Blackwell hardware:
+//
+//   * warp 0, one thread: TMA producer.  Per K slice of 64 it loads a
+//     128 x 64 slice of the MMA's A operand and a BN x 64 slice of its B
+//     operand, 128-byte swizzled, into a STAGES-deep shared-memory ring; each
+//     stage has a "full" mbarrier (TMA transaction bytes) and an "empty"
+//     mbarrier (released by the MMA's commit).
+//   * warp 1: allocates tensor memory (two BN-column FP32 accumulators of
+//     128 lanes), and one thread issues tcgen05.mma (128 x BN x 16 each, four
+//     per stage) and tcgen05.commit.
+//   * warps 2-5: epilogue.  Each warp reads its 32 accumulator lanes with
+//     tcgen05.ld and writes FP32 results to C; the accumulator is double
+//     buffered so the epilogue of one tile overlaps the next tile's main loop.
+//
+// Operand roles.  Without swap, the MMA's A operand is A (K contiguous:
+// "K-major") and its B operand is B (N contiguous: "MN-major"), and
+// tensor-memory lane = row of C.  With swap (small M) the kernel computes
+// C^T = B^T A^T: the MMA's A operand is B (MN-major, 128 columns of C per
+// tile) and its B operand is A (K-major, BN rows of C), and lane = column
+// of C, so the epilogue's stores stay coalesced.
+//
+// Edges.  Loads never need a guard: TMA fills out-of-range elements of a box
+// with zeros, so a K tail multiplies zeros and an M or N tail produces rows or
+// columns that are never stored.  The epilogue decides once per 32-column
+// chunk whether the chunk is whole (vector stores) or ragged (element-masked
+// stores) -- a separate edge path instead of a guard in the inner loop, as
+// "matmul_registers.cu" recommends for ragged shapes.
+//
+// Split-K.  A unit of work is (tile, K slice).  Each slice writes its FP32
+// partial tile to a workspace and bumps a per-(tile, warp quarter) counter;
+// the quarter that arrives last sums the partials in slice order 0..S-1 (a
+// fixed order, so results do not depend on timing) and writes C.
+//
+// Waits.  Every mbarrier wait gives up after kWaitLimitNs, sets a bit in the
+// device error word and makes the whole CTA leave its loops; before exiting,
+// the producer waits (bounded) for its own TMA copies and the MMA thread for
+// its own MMAs, and tensor memory is freed on every path.
+
+#include <cstdio>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+__device__ uint32_t g_tc_error;  // device error word; bits below
+
+constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s for copies already in flight
+constexpr int kThreads = 192;
+constexpr int kUmmaK = 16;
+
+struct TcArgs {
+    float* C;
+    int64_t ldc;
+    int32_t M, N;
+    int32_t tiles_p, tiles_q;   // tiles along the MMA M side / N side
+    int32_t num_units;          // tiles * splits
+    int32_t splits, kb_total, kb_per_split;
+    int32_t group;
+    int32_t vec_store;          // C rows are 16-byte aligned: float4 stores allowed
+    uint32_t idesc;
+    float* ws;
+    uint32_t* counters;
+};
+
+template <int BN, bool SWAP>
+struct TcTraits {
+    static constexpr int kPBytes = kTcBM * kTcBK * 2;   // MMA A operand per stage
+    static constexpr int kQBytes = BN * kTcBK * 2;      // MMA B operand per stage
+    static constexpr int kStageBytes = kPBytes + kQBytes;
+    static constexpr int kStages = (BN == 256) ? 4 : (BN == 128) ? 6 : (BN == 64) ? 8
+                                 : (BN == 32) ? 9 : 10;
+    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;  // two accumulators
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
+                                      kNumBars * 8 + 16;
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+    static_assert(SWAP ? (BN <= 64) : (BN >= 64 && BN % 64 == 0), "operand box shapes");
+    static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "tensor memory");
+    static_assert(kPBytes % 1024 == 0 && kQBytes % 1024 == 0, "1024-byte swizzle atoms");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
+    static_assert(kSmemBytes > 114 * 1024, "one CTA per SM keeps tensor memory uncontended");
+};
+
+struct WaitCtx {
+    volatile uint32_t* abort_flag;
+};
+
+// Bounded wait: true when the phase of the given parity completed; false when
+// the CTA is aborting (this wait gave up, or another role did).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                           uint32_t err_bit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *w.abort_flag = 1;
+            atomicOr(&g_tc_error, err_bit);
+            return false;
+        }
+    }
+}
+
+// Short bounded wait used only while draining before exit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kDrainLimitNs) {
+            atomicOr(&g_tc_error, kErrDrain);
+            return;
+        }
+    }
+}
+
+// Unit -> (tile along MMA M side, tile along MMA N side, K slice).  Tiles are
+// visited in groups of `group` tiles along the M side, column by column, so
+// the CTAs working at one time share operand panels in L2.
+__device__ __forceinline__ void unit_coords(const TcArgs& a, int u, int& pb, int& qb, int& split) {
+    const int tile = u / a.splits;
+    split = u - tile * a.splits;
+    const int group_tiles = a.group * a.tiles_q;
+    const int g = tile / group_tiles;
+    const int first_p = g * a.group;
+    const int gsz = min(a.tiles_p - first_p, a.group);
+    const int r = tile - g * group_tiles;
+    pb = first_p + r % gsz;
+    qb = r / gsz;
+}
+
+// ---- epilogue stores ----------------------------------------------------------
+
+// W accumulator values of this thread's lane (`p` along the MMA M side),
+// columns q0..q0+W-1 along the MMA N side.
+template <bool SWAP, int W>
+__device__ __forceinline__ void store_chunk(const TcArgs& a, const float (&v)[W], int p, int q0) {
+    if (!SWAP) {
+        // lane = row of C, chunk = W consecutive columns of that row.
+        if (p >= a.M) return;
+        float* dst = a.C + static_cast<int64_t>(p) * a.ldc + q0;
+        if (a.vec_store && q0 + W <= a.N) {
+#pragma unroll
+            for (int i = 0; i < W; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i)
+                if (q0 + i < a.N) dst[i] = v[i];
+        }
+    } else {
+        // lane = column of C, chunk = W consecutive rows; lanes of a warp
+        // write 32 consecutive floats of each row.
+        if (p >= a.N) return;
+        float* dst = a.C + static_cast<int64_t>(q0) * a.ldc + p;
+        if (q0 + W <= a.M) {
+#pragma unroll
+            for (int i = 0; i < W; ++i) dst[static_cast<int64_t>(i) * a.ldc] = v[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i)
+                if (q0 + i < a.M) dst[static_cast<int64_t>(i) * a.ldc] = v[i];
+        }
+    }
+}
+
+// ---- the kernel ---------------------------------------------------------------
+
+template <int BN, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q,
+               const TcArgs args) {
+    using T = TcTraits<BN, SWAP>;
+    constexpr int S = T::kStages;
+    constexpr int CW = BN < 32 ? BN : 32;   // accumulator columns per tensor-memory load
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t smem_base = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * T::kStageBytes);
+    const uint32_t bar_base = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return bar_base + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bar_base + 8u * (2 * S + 2 + b); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * S + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + T::kNumBars);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);   // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_p);
+        tma_prefetch_map(&map_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), T::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtx wctx{abort_flag};
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;   // per-stage: armed at least once / parity
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < args.num_units; u += gridDim.x) {
+                int pb, qb, split;
+                unit_coords(args, u, pb, qb, split);
+                const int kb0 = split * args.kb_per_split;
+                const int kb1 = min(kb0 + args.kb_per_split, args.kb_total);
+                const int p0 = pb * kTcBM, q0 = qb * BN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(empty_bar(stage), phase ^ 1u, wctx, kErrProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, T::kStageBytes);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    const uint32_t sp = smem_base + stage * T::kStageBytes;
+                    const uint32_t sq = sp + T::kPBytes;
+                    const int k0 = kb * kTcBK;
+                    if (!SWAP) {
+                        tma_load_2d(sp, &map_p, fb, k0, p0);                 // A: box {64 k, 128 rows}
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)                    // B: boxes {64 cols, 64 k}
+                            tma_load_2d(sq + j * 8192, &map_q, fb, q0 + 64 * j, k0);
+                    } else {
+                        tma_load_2d(sp, &map_p, fb, p0, k0);                 // B: boxes {64 cols, 64 k}
+                        tma_load_2d(sp + 8192, &map_p, fb, p0 + 64, k0);
+                        tma_load_2d(sq, &map_q, fb, k0, q0);                 // A: box {64 k, BN rows}
+                    }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy this thread issued has landed before the CTA exits.
+            for (int s = 0; s < S; ++s)
+                if (armed & (1u << s)) drain_wait(full_bar(s), (armed_parity >> s) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < args.num_units; u += gridDim.x) {
+                int pb, qb, split;
+                unit_coords(args, u, pb, qb, split);
+                const int kb0 = split * args.kb_per_split;
+                const int kb1 = min(kb0 + args.kb_per_split, args.kb_total);
+                if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, wctx, kErrMma)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_phase(full_bar(stage), phase, wctx, kErrMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sp = smem_base + stage * T::kStageBytes;
+                    const uint32_t sq = sp + T::kPBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcBK / kUmmaK; ++kk) {
+                        // K-major operand: next 16 k are 32 bytes further along each
+                        // 128-byte row.  MN-major operand: next 16 k are 16 rows of
+                        // 128 bytes further.
+                        const uint64_t adesc = SWAP ? smem_desc_sw128(sp + kk * 2048, 8192, 1024)
+                                                    : smem_desc_sw128(sp + kk * 32, 16, 1024);
+                        const uint64_t bdesc = SWAP ? smem_desc_sw128(sq + kk * 32, 16, 1024)
+                                                    : smem_desc_sw128(sq + kk * 2048, 8192, 1024);
+                        tc_mma_f16(d_tmem, adesc, bdesc, args.idesc,
+                                   (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));   // stage is free once these MMAs finish
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(accf_bar(acc));          // accumulator ready for the epilogue
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // Every MMA this thread issued has finished before tensor memory is freed.
+            tc_commit(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue ----------------------------------
+        const int quarter = warp & 3;                 // tensor-memory lanes 32*quarter ..
+        const int row = quarter * 32 + lane;          // lane within the 128-row tile
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
+            int pb, qb, split;
+            unit_coords(args, u, pb, qb, split);
+            bool ok = wait_phase(accf_bar(acc), acc_phase, wctx, kErrEpilogue);
+            if (!__all_sync(0xffffffffu, ok)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t t_lane = tmem_base + static_cast<uint32_t>(acc * BN) +
+                                    (static_cast<uint32_t>(quarter * 32) << 16);
+            const int p = pb * kTcBM + row;
+            const int q0 = qb * BN;
+            const int tile = u / args.splits;
+            float* slot = (args.splits > 1)
+                ? args.ws + (static_cast<int64_t>(tile) * args.splits + split) * (kTcBM * BN)
+                : nullptr;
+#pragma unroll 1
+            for (int c = 0; c < BN / CW; ++c) {
+                uint32_t r[CW];
+                tmem_ld_lane_cols<CW>(t_lane + c * CW, r);
+                tmem_wait_ld();
+                if (c == BN / CW - 1) {
+                    // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                }
+                float v[CW];
+#pragma unroll
+                for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+                if (args.splits == 1) {
+                    store_chunk<SWAP, CW>(args, v, p, q0 + c * CW);
+                } else {
+                    // partial tile, laid out [column][row] so a warp's stores are
+                    // 32 consecutive floats
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) slot[(c * CW + i) * kTcBM + row] = v[i];
+                }
+            }
+            if (args.splits > 1) {
+                __threadfence();
+                __syncwarp();
+                uint32_t last = 0;
+                if (lane == 0) {
+                    uint32_t* cnt = args.counters + tile * 4 + quarter;
+                    last = (atomicAdd(cnt, 1u) == static_cast<uint32_t>(args.splits - 1)) ? 1u : 0u;
+                    if (last) atomicExch(cnt, 0u);   // ready for the next launch
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    const float* base = args.ws + static_cast<int64_t>(tile) * args.splits * (kTcBM * BN);
+#pragma unroll 1
+                    for (int c = 0; c < BN / CW; ++c) {
+                        float v[CW];
+#pragma unroll
+                        for (int i = 0; i < CW; ++i) v[i] = 0.0f;
+                        for (int s = 0; s < args.splits; ++s) {
+                            const float* src = base + static_cast<int64_t>(s) * (kTcBM * BN);
+#pragma unroll
+                            for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
+                        }
+                        store_chunk<SWAP, CW>(args, v, p, q0 + c * CW);
+                    }
+                }
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, T::kTmemCols);
+    }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+bool tc_config_supported(int bn, int swap) {
+    if (swap) return bn == 16 || bn == 32 || bn == 64;
+    return bn == 64 || bn == 128 || bn == 256;
+}
+
+cudaError_t tc_error_word(uint32_t** ptr) {
+    return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_tc_error);
+}
+
+static bool encode_map(EncodeTiledFn encode, CUtensorMap* map, int fmt, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box_inner,
+                       uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld_elems * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool SWAP>
+static cudaError_t launch_cfg(const TcLaunch& L, const CUtensorMap& mp, const CUtensorMap& mq,
+                              const TcArgs& args, cudaStream_t stream) {
+    using T = TcTraits<BN, SWAP>;
+    auto kern = tc_gemm_kernel<BN, SWAP>;
+    // The attribute is per device; setting it every call is cheap and keeps
+    // multi-device use correct.
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<L.grid, kThreads, T::kSmemBytes, stream>>>(mp, mq, args);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t stream) {
+    if (!tc_config_supported(L.bn, L.swap)) return cudaErrorInvalidValue;
+    // A: {K, M} (K contiguous); B: {N, K} (N contiguous).
+    CUtensorMap map_a, map_b;
+    const uint32_t a_rows = L.swap ? static_cast<uint32_t>(L.bn) : kTcBM;
+    if (!encode_map(encode, &map_a, L.fmt, L.A, L.K, L.M, L.lda, 64, a_rows))
+        return cudaErrorInvalidValue;
+    if (!encode_map(encode, &map_b, L.fmt, L.B, L.N, L.K, L.ldb, 64, 64))
+        return cudaErrorInvalidValue;
+
+    TcArgs a;
+    a.C = L.C;
+    a.ldc = L.ldc;
+    a.M = static_cast<int32_t>(L.M);
+    a.N = static_cast<int32_t>(L.N);
+    const int64_t pe = L.swap ? L.N : L.M;
+    const int64_t qe = L.swap ? L.M : L.N;
+    a.tiles_p = static_cast<int32_t>(ceil_div(pe, kTcBM));
+    a.tiles_q = static_cast<int32_t>(ceil_div(qe, L.bn));
+    a.kb_total = static_cast<int32_t>(ceil_div(L.K, kTcBK));
+    a.splits = L.splits;
+    a.kb_per_split = static_cast<int32_t>(ceil_div(a.kb_total, L.splits));
+    a.num_units = a.tiles_p * a.tiles_q * L.splits;
+    a.group = L.group;
+    a.vec_store = ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0 && (L.ldc & 3) == 0) ? 1 : 0;
+    a.idesc = idesc_f16_f32(static_cast<uint32_t>(L.fmt), L.swap != 0, L.swap == 0, kTcBM,
+                            static_cast<uint32_t>(L.bn));
+    a.ws = L.ws;
+    a.counters = L.counters;
+
+    const CUtensorMap& mp = L.swap ? map_b : map_a;
+    const CUtensorMap& mq = L.swap ? map_a : map_b;
+    if (!L.swap) {
+        switch (L.bn) {
+            case 64: return launch_cfg<64, false>(L, mp, mq, a, stream);
+            case 128: return launch_cfg<128, false>(L, mp, mq, a, stream);
+            case 256: return launch_cfg<256, false>(L, mp, mq, a, stream);
+        }
+    } else {
+        switch (L.bn) {
+            case 16: return launch_cfg<16, true>(L, mp, mq, a, stream);
+            case 32: return launch_cfg<32, true>(L, mp, mq, a, stream);
+            case 64: return launch_cfg<64, true>(L, mp, mq, a, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gb300

@@ -1,0 +1,178 @@
+/*
+ * gb300gemm.h -- C ABI of the GB300 (sm_103a) dense matrix multiply.
+ *
+ * Operation (every GEMM entry point): C = A x B, overwriting C, with
+ *
+ *     C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j]
+ *
+ * for A of M x K, B of K x N and C of M x N ("Tensor cores and matrix
+ * operations", section "Traditional Approach: Element-by-Element").  No
+ * alpha, beta or bias.  All three matrices are row-major; a leading
+ * dimension is the row stride of the full matrix in elements, not of a tile
+ * ("04-wmma-matmul" code example, comment on load_matrix_sync), so element
+ * (i, k) of A is A[i * lda + k] and lda >= K, ldb >= N, ldc >= N.
+ *
+ * Arithmetic: the 16-bit entry points multiply FP16 or BF16 inputs and
+ * accumulate in FP32 ("CUDA-Practice 09", the sections on mixed precision:
+ * 16-bit inputs halve the bytes moved, FP32 accumulation avoids the rounding
+ * of long 16-bit sums).  The FP32 entry point computes in FP32 on the CUDA
+ * cores ("matmul_registers.cu", the register-tiled SGEMM it builds up).
+ * Summation order inside a sum is unspecified; results meet
+ * max|C - C_exact| <= 1e-3 sqrt(K) max|A| max|B| and a relative Frobenius
+ * error <= 1e-4, and are bit-exact whenever every product and partial sum is
+ * an integer below 2^24.
+ *
+ * Memory and ownership: A, B and C are DEVICE pointers owned by the caller
+ * on the current CUDA device; the library never allocates, frees or copies
+ * them.  C must not overlap A or B.  The library owns a small per-device,
+ * per-stream split-K workspace (partial tiles + tile counters) that it
+ * allocates on first use and grows as needed; gemm_release_workspace() frees
+ * it.
+ *
+ * Streams: every call enqueues its kernels on `stream` (NULL = the legacy
+ * default stream) and returns without synchronising.  A fault in a kernel
+ * surfaces at the caller's next synchronisation; a pipeline wait that ran out
+ * of time (see gemm_device_error) is recorded on the device instead of
+ * hanging it.
+ *
+ * Errors: every function returns a gemm_status_t and never prints or exits.
+ * Argument errors are found on the host before anything is enqueued.
+ *
+ * Thread safety: calls from several host threads are safe.  Calls on
+ * different streams of one device each use their own workspace.
+ */
+#ifndef GB300GEMM_H
+#define GB300GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL selects the default stream. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,      /* null pointer with M, N > 0; negative dim; ld too small;
+                                        a dimension above 2^31 - 1                       */
+    GEMM_ERR_OVERLAP = 2,            /* C's span overlaps A's or B's                      */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3     */
+    GEMM_ERR_LAUNCH = 4,             /* a kernel launch failed (see gemm_last_cuda_error) */
+    GEMM_ERR_DEVICE_TIMEOUT = 5,     /* a pipeline wait in a kernel gave up (device flag) */
+    GEMM_ERR_CUDA = 6,               /* another CUDA runtime call failed                  */
+    GEMM_ERR_OUT_OF_MEMORY = 7       /* the split-K workspace could not be allocated       */
+} gemm_status_t;
+
+/*
+ * gemm_f16f32 -- C (FP32) = A (FP16) x B (FP16), FP32 accumulate, tensor cores.
+ *
+ * A: const __half*, M x K, row stride lda.  B: const __half*, K x N, row
+ * stride ldb.  C: float*, M x N, row stride ldc.
+ * Path: when A and B start on 16-byte boundaries and lda, ldb are multiples of
+ * 8, a TMA + tcgen05.mma kernel (accumulators in tensor memory); otherwise a
+ * CUDA-core kernel with the same FP32 accumulation.  Shapes that are not a
+ * whole number of tiles are handled by the kernels' edge paths.
+ * M == 0 or N == 0: nothing is enqueued.  K == 0: C is filled with zeros (the
+ * empty sum).
+ */
+gemm_status_t gemm_f16f32(const void *A, const void *B, float *C,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc,
+                          gemm_stream_t stream);
+
+/* gemm_bf16f32 -- as gemm_f16f32, with BF16 (__nv_bfloat16) A and B. */
+gemm_status_t gemm_bf16f32(const void *A, const void *B, float *C,
+                           int64_t M, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldc,
+                           gemm_stream_t stream);
+
+/*
+ * sgemm_f32 -- C = A x B, all FP32, FP32 fused multiply-add on the CUDA
+ * cores (no TF32).  Layout, ownership, streams and degenerate shapes as
+ * gemm_f16f32.  Path: a register-tiled kernel (8 x 8 outputs per thread,
+ * float4 global loads, A staged transposed in shared memory) when A, B and C
+ * start on 16-byte boundaries and lda, ldb, ldc are multiples of 4; a guarded
+ * scalar kernel otherwise.  Never returns an alignment error.
+ */
+gemm_status_t sgemm_f32(const float *A, const float *B, float *C,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc,
+                        gemm_stream_t stream);
+
+/*
+ * Options for gemm_ex.  Zero-initialise and set what you need; a zero field
+ * means "let the planner choose".
+ *   dtype     0 = FP16, 1 = BF16, 2 = FP32 (sgemm_f32's kernels).
+ *   tile_n    dtype 0/1: tensor-core tile width along the MMA's N side: 16,
+ *             32, 64, 128 or 256 (16..64 only with swap_ab = 1; 64..256
+ *             without).  dtype 2: 128 -> 128x128 SGEMM tiles, 64 -> 128x64,
+ *             32 -> 64x64.
+ *   split_k   number of K slices, each reduced in a fixed order (1..64).
+ *   swap_ab   -1 = planner, 0 = never, 1 = compute C^T = B^T A^T so that N
+ *             runs along the 128-row MMA side (for small M).
+ *   generic   1 = force the CUDA-core kernel (any alignment).
+ *   group_m   tiles per raster group along the 128-row side (0 = planner).
+ * Invalid combinations return GEMM_ERR_INVALID_VALUE.
+ */
+typedef struct {
+    int32_t dtype;
+    int32_t tile_n;
+    int32_t split_k;
+    int32_t swap_ab;
+    int32_t generic;
+    int32_t group_m;
+    int32_t reserved[2];
+} gemm_options_t;
+
+/* gemm_ex -- the same operation with an explicit plan (tests and tuning). */
+gemm_status_t gemm_ex(const void *A, const void *B, float *C,
+                      int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc,
+                      const gemm_options_t *options, gemm_stream_t stream);
+
+/*
+ * gemm_plan_describe -- the plan gemm_f16f32 / gemm_bf16f32 / sgemm_f32 would
+ * use for these arguments on the current device, as text written to buf
+ * (always NUL-terminated when size > 0).  Pointers are not dereferenced; only
+ * their alignment is read.  Returns the status the call would return from
+ * argument checking.
+ */
+gemm_status_t gemm_plan_describe(int32_t dtype, const void *A, const void *B, const float *C,
+                                 int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldc,
+                                 const gemm_options_t *options, char *buf, int64_t size);
+
+/*
+ * gemm_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error flag.  Returns GEMM_ERR_DEVICE_TIMEOUT if any
+ * kernel since the last call gave up a pipeline wait (it then wrote no
+ * trustworthy output), GEMM_ERR_CUDA if the synchronisation failed, else
+ * GEMM_OK.
+ */
+gemm_status_t gemm_device_error(gemm_stream_t stream);
+
+/* gemm_release_workspace -- frees the split-K workspaces of the current
+ * device after synchronising the device.  Later calls allocate again. */
+gemm_status_t gemm_release_workspace(void);
+
+/* Text for a status code (static storage). */
+const char *gemm_status_string(gemm_status_t status);
+
+/* Text of the last CUDA error seen by this host thread inside the library
+ * (static thread-local storage; "" if none). */
+const char *gemm_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t gemm_version(void);
+
+/* Number of kernel launches this host thread has enqueued through the library
+ * since it loaded (monotonic counter, for accounting in benchmarks). */
+int64_t gemm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300GEMM_H */

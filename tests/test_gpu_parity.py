@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.  Needs a GB300 and the built library."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_gemm_tensor_tcgen05_gb300 import inputs
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    from dense_gemm_tensor_tcgen05_gb300 import build
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    build.build()
+    oracle.build()
+    g.lib()
+    yield
+
+
+# ---- exact cases first: small integers are exact in every summation order ----
+
+EXACT_SHAPES = [(1, 1, 1), (7, 9, 5), (128, 256, 64), (128, 64, 64), (100, 300, 70),
+                (256, 512, 1024), (129, 257, 65), (8, 200, 130), (33, 1000, 129)]
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("shape", EXACT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_int_exact_default_plan(dt, shape):
+    M, N, K = shape
+    gu.check_full(dt, "small_int", M, N, K, exact=True)
+
+
+TC_CONFIGS = [
+    dict(tile_n=256, swap_ab=0, split_k=1), dict(tile_n=128, swap_ab=0, split_k=1),
+    dict(tile_n=64, swap_ab=0, split_k=1), dict(tile_n=16, swap_ab=1, split_k=1),
+    dict(tile_n=32, swap_ab=1, split_k=1), dict(tile_n=64, swap_ab=1, split_k=1),
+    dict(tile_n=256, swap_ab=0, split_k=3), dict(tile_n=128, swap_ab=0, split_k=2),
+    dict(tile_n=64, swap_ab=0, split_k=7), dict(tile_n=16, swap_ab=1, split_k=4),
+    dict(tile_n=64, swap_ab=1, split_k=5), dict(tile_n=128, swap_ab=0, split_k=1, group_m=1),
+    dict(tile_n=256, swap_ab=0, split_k=1, group_m=3),
+]
+
+
+def _cfg_id(c):
+    return "-".join(f"{k}{v}" for k, v in c.items())
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("cfg", TC_CONFIGS, ids=_cfg_id)
+@pytest.mark.parametrize("shape", [(300, 520, 700), (1, 129, 1000), (640, 512, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tensor_core_configs_exact(dt, cfg, shape):
+    M, N, K = shape
+    gu.check_full(dt, "small_int", M, N, K, exact=True, **cfg)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("cfg", TC_CONFIGS, ids=_cfg_id)
+def test_tensor_core_configs_random(dt, cfg):
+    gu.check_full(dt, "uniform", 333, 450, 1111, seed=5, **cfg)
+
+
+@pytest.mark.parametrize("cfg", [dict(tile_n=128), dict(tile_n=64), dict(tile_n=32)],
+                         ids=_cfg_id)
+@pytest.mark.parametrize("shape", [(300, 520, 700), (9, 7, 3), (130, 200, 1)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_sgemm_tiles_exact(cfg, shape):
+    M, N, K = shape
+    gu.check_full("f32", "small_int", M, N, K, exact=True, **cfg)
+
+
+# ---- the workloads' configurations ------------------------------------------
+
+def test_config_f16_1024_uniform_full():
+    gu.check_full("f16", "uniform", 1024, 1024, 1024, seed=1234)
+
+
+def test_config_sgemm_1024_uniform_full():
+    gu.check_full("f32", "uniform", 1024, 1024, 1024, seed=1235)
+
+
+def test_config_sgemm_4096_uniform_sampled():
+    M = N = K = 4096
+    A, B = gu.make_inputs("f32", "uniform", M, N, K, 1236)
+    C = gu.run_gpu("f32", A, B, M, N, K)
+    cmp = gu.check_sampled("f32", A, B, C, M, N, K)
+    assert cmp.ok, str(cmp)
+    assert np.isfinite(C).all()
+
+
+def test_config_f16_2048_normal_full():
+    gu.check_full("f16", "normal", 2048, 2048, 2048, seed=1237)
+
+
+def test_config_bf16_8192_normal_sampled():
+    M = N = K = 8192
+    A, B = gu.make_inputs("bf16", "normal", M, N, K, 1238, sigma=1 / math.sqrt(K))
+    C = gu.run_gpu("bf16", A, B, M, N, K)
+    assert np.isfinite(C).all()
+    cmp = gu.check_sampled("bf16", A, B, C, M, N, K)
+    assert cmp.ok, str(cmp)
+
+
+@pytest.mark.parametrize("shape", [(4000, 3000, 1000), (16384, 128, 4096), (8, 8192, 8192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_config_ragged_skinny(shape):
+    M, N, K = shape
+    A, B = gu.make_inputs("f16", "uniform", M, N, K, 1239)
+    C = gu.run_gpu("f16", A, B, M, N, K)
+    assert np.isfinite(C).all()
+    if M * N * K <= 6e8:
+        R = oracle.gemm("f16", A, B)
+        cmp = oracle.compare(C, R, K, inputs.bits_abs_max(A, "f16"), inputs.bits_abs_max(B, "f16"))
+    else:
+        cmp = gu.check_sampled("f16", A, B, C, M, N, K, band=32)
+    assert cmp.ok, str(cmp)
+
+
+@pytest.mark.parametrize("shape", [(4000, 3000, 1000), (16384, 128, 4096), (8, 8192, 8192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_config_ragged_skinny_small_int_exact(shape):
+    M, N, K = shape
+    A, B = gu.make_inputs("f16", "small_int", M, N, K, 0)
+    C = gu.run_gpu("f16", A, B, M, N, K)
+    cmp = gu.check_sampled("f16", A, B, C, M, N, K, band=32)
+    assert cmp.ok and cmp.exact, str(cmp)
+
+
+# ---- edges and degenerate cases ----------------------------------------------
+
+EDGE = [1, 2, 7, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("aligned", [True, False], ids=["aligned_ld", "tight_ld"])
+def test_edge_sweep_small_int(dt, aligned):
+    rng = np.random.default_rng(7)
+    align = (8 if dt != "f32" else 4) if aligned else 0
+    for _ in range(40):
+        M, N, K = (int(x) for x in rng.choice(EDGE, size=3))
+        gu.check_full(dt, "small_int", M, N, K, exact=True, align_ld=align)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_tiny_shapes_tensor_core_path(dt):
+    # every (M, N, K) in 1..9 through the TMA + tcgen05 kernels (padded rows),
+    # with and without swap
+    for M in range(1, 10):
+        for N in range(1, 10, 2):
+            for K in range(1, 10, 2):
+                gu.check_full(dt, "small_int", M, N, K, exact=True, align_ld=8)
+                gu.check_full(dt, "uniform", M, N, K, seed=K, align_ld=8, swap_ab=0)
+
+
+@pytest.mark.parametrize("dt", ["f16", "f32"])
+def test_tiny_shapes_bruteforce(dt):
+    for M in range(1, 10, 2):
+        for N in range(1, 10, 3):
+            for K in range(1, 10, 4):
+                gu.check_full(dt, "uniform", M, N, K, seed=M * 100 + N * 10 + K)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+def test_padded_leading_dimensions(dt):
+    # padding holds poison; a kernel that reads or writes past K or N fails
+    gu.check_full(dt, "small_int", 200, 300, 150, exact=True, pad=(8, 16, 12))
+    gu.check_full(dt, "uniform", 131, 77, 259, seed=3, pad=(24, 8, 5))
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+def test_misaligned_pointers_and_leading_dims(dt):
+    M, N, K = 70, 90, 50          # K, N not multiples of 8: no TMA, no float4
+    A, B = gu.make_inputs(dt, "small_int", M, N, K, 0)
+    C = gu.run_gpu(dt, A, B, M, N, K, offsets=(1, 3, 1))
+    R = oracle.gemm(dt, A, B)
+    assert np.array_equal(C, R.astype(np.float32))
+
+
+def test_k_zero_gives_zeros():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    for dt, fn in (("f16", g.gemm_f16f32), ("bf16", g.gemm_bf16f32), ("f32", g.sgemm_f32)):
+        C = torch.full((5, 7), float("nan"), device="cuda")
+        fn(0, 0, C.data_ptr(), 5, 7, 0, 0, 7, 7, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert torch.all(C == 0).item(), dt
+
+
+def test_m_or_n_zero_is_a_no_op():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    before = g.gemm_launch_count()
+    g.gemm_f16f32(0, 0, 0, 0, 16, 16, 16, 16, 16)
+    g.gemm_bf16f32(0, 0, 0, 16, 0, 16, 16, 0, 0)
+    torch.cuda.synchronize()
+    assert g.gemm_launch_count() == before
+
+
+def test_golden_fixtures_on_gpu():
+    import os
+    gold = os.path.join(os.path.dirname(__file__), "golden")
+
+    def load(name, M, N):
+        v = [float(l) for l in open(os.path.join(gold, name)) if not l.startswith("#")]
+        return np.array(v).reshape(M, N)
+
+    A, B = gu.make_inputs("f16", "small_int", 12, 10, 9, 0)
+    C = gu.run_gpu("f16", A, B, 12, 10, 9)
+    assert np.array_equal(C, load("small_int_12x10x9.txt", 12, 10).astype(np.float32))
+    A, B = gu.make_inputs("f16", "mod_pattern", 16, 16, 16, 0)
+    C = gu.run_gpu("f16", A, B, 16, 16, 16)
+    cmp = oracle.compare(C, load("mod_pattern_16.txt", 16, 16), 16, 0.5, 0.5)
+    assert cmp.ok, str(cmp)
+
+
+# ---- determinism, streams, host buffers --------------------------------------------
+
+@pytest.mark.parametrize("cfg", [dict(), dict(tile_n=64, swap_ab=1, split_k=6),
+                                 dict(tile_n=128, swap_ab=0, split_k=5)], ids=_cfg_id)
+def test_repeat_runs_bit_identical(cfg):
+    A, B = gu.make_inputs("bf16", "normal", 96, 1000, 2048, 11)
+    Cs = [gu.run_gpu("bf16", A, B, 96, 1000, 2048, **cfg) for _ in range(4)]
+    for C in Cs[1:]:
+        assert np.array_equal(C, Cs[0])
+
+
+def test_concurrent_streams_split_k():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    M, N, K = 8, 4096, 8192
+    A, B = gu.make_inputs("f16", "small_int", M, N, K, 0)
+    Ad, Bd = gu.to_device(A, "f16"), gu.to_device(B, "f16")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    outs = [torch.full((M, N), float("nan"), device="cuda") for _ in streams]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for s, C in zip(streams, outs):
+            g.gemm_f16f32(Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, K, N, N,
+                          s.cuda_stream)
+    torch.cuda.synchronize()
+    g.gemm_device_error()
+    R = oracle.gemm("f16", A, B).astype(np.float32)
+    for C in outs:
+        assert np.array_equal(C.cpu().numpy(), R)
+
+
+def test_matmul_with_host_buffers():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    A, B = gu.make_inputs("bf16", "uniform", 300, 200, 500, 21)
+    At = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Bt = torch.from_numpy(B.view(np.int16)).view(torch.bfloat16).pin_memory()
+    C = g.matmul(At, Bt)
+    assert not C.is_cuda
+    R = oracle.gemm("bf16", A, B)
+    cmp = oracle.compare(C.numpy(), R, 500, inputs.bits_abs_max(A, "bf16"), inputs.bits_abs_max(B, "bf16"))
+    assert cmp.ok, str(cmp)
+
+
+def test_plan_describe_routes():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+
+    def plan(dt, M, N, K):
+        A = torch.empty((M, K), dtype=gu.torch_dtype(dt), device="cuda")
+        B = torch.empty((K, N), dtype=gu.torch_dtype(dt), device="cuda")
+        return g.plan(A, B)
+    assert plan("bf16", 8192, 8192, 8192).startswith("tcgen05")
+    assert "swap=1" in plan("f16", 8, 8192, 8192)
+    assert plan("f32", 4096, 4096, 4096).startswith("sgemm")
+    assert plan("f16", 10, 10, 7).startswith("generic")   # lda = 7: no TMA
