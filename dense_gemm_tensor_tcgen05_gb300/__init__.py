@@ -22,7 +22,7 @@ import threading
 
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
-    "gemm_plan_describe", "gemm_device_error", "gemm_release_workspace", "gemm_version",
+    "gemm_ex_noalloc", "gemm_plan_describe", "gemm_device_error", "gemm_release_workspace", "gemm_version",
     "gemm_launch_count", "matmul", "plan", "GemmOptions", "STATUS", "EXPORTED_SYMBOLS",
 ]
 
@@ -44,7 +44,7 @@ STATUS = {
 EXPORTED_SYMBOLS = (
     "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex", "gemm_plan_describe",
     "gemm_device_error", "gemm_release_workspace", "gemm_status_string",
-    "gemm_last_cuda_error", "gemm_version", "gemm_launch_count",
+    "gemm_last_cuda_error", "gemm_version", "gemm_launch_count", "gemm_ex_noalloc",
 )
 
 
@@ -88,6 +88,9 @@ def lib() -> ctypes.CDLL:
             L.gemm_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                   ctypes.POINTER(GemmOptions), vp]
             L.gemm_ex.restype = ctypes.c_int
+            L.gemm_ex_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                          ctypes.POINTER(GemmOptions), vp]
+            L.gemm_ex_noalloc.restype = ctypes.c_int
             L.gemm_plan_describe.argtypes = [ctypes.c_int32, vp, vp, vp, i64, i64, i64, i64, i64,
                                              i64, ctypes.POINTER(GemmOptions), ctypes.c_char_p, i64]
             L.gemm_plan_describe.restype = ctypes.c_int
@@ -141,6 +144,14 @@ def gemm_ex(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, 
             dtype: int, stream: int = 0, **opts) -> None:
     o = _options(dtype, **opts)
     _check(lib().gemm_ex(A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o), stream or None))
+
+
+def gemm_ex_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                    ldc: int, dtype: int, stream: int = 0, **opts) -> None:
+    """gemm_ex without device allocations: split-K scratch lives in a fixed
+    8 MiB array inside the library (see include/gb300gemm.h)."""
+    o = _options(dtype, **opts)
+    _check(lib().gemm_ex_noalloc(A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o), stream or None))
 
 
 def gemm_plan_describe(dtype: int, A: int, B: int, C: int, M: int, N: int, K: int, lda: int,

@@ -494,3 +494,131 @@ int32_t gemm_version(void) { return 100; }
 int64_t gemm_launch_count(void) { return t_launches; }
 
 }  // extern "C"
+
+// ---- allocation-free entry point ------------------------------------------------
+//
+// gemm_ex_noalloc serves callers that must not allocate device memory after
+// start-up: applications that hand the GPU's memory to their own pool and
+// account for every byte, and latency-critical loops in which a cudaMalloc
+// or cudaFree (which can synchronise the device) is not acceptable.  It runs
+// the same kernels as gemm_ex; the only difference is where the split-K
+// tensor-core kernel keeps its scratch (partial tiles and arrival counters):
+// in the file-scope array below instead of a workspace allocated on first use.
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = GEMM_NOALLOC_SCRATCH_BYTES;
+constexpr size_t kNoallocCounterBytes = 64 * 1024;   // counters for up to 4096 tiles
+constexpr int kNoallocMaxDevices = 64;
+
+// Every device that loads this library holds this array until the process
+// exits.  In host code the name is only a stand-in: its device address comes
+// from cudaGetSymbolAddress, once per device, in noalloc_scratch() below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoallocMaxDevices];   // device address per device, or null
+
+// Device address of the scratch array on `dev` (which must be current).
+gemm_status_t noalloc_scratch(int dev, unsigned char** out) {
+    if (dev < 0 || dev >= kNoallocMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            note_cuda_error(e, "cudaGetSymbolAddress(no-alloc scratch)");
+            return GEMM_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_addr[dev]);
+    return GEMM_OK;
+}
+
+// Current device, its SM count, and the compute-capability check, read
+// through device attributes (no library-side caches are filled).
+gemm_status_t noalloc_device(int* dev, int* sms) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaGetDevice");
+        return GEMM_ERR_CUDA;
+    }
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess) {
+        note_cuda_error(e, "cudaDeviceGetAttribute");
+        return GEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C, int64_t M,
+                                         int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                         int64_t ldc, const gemm_options_t* options,
+                                         gemm_stream_t stream_handle) {
+    if (!options) return GEMM_ERR_INVALID_VALUE;
+    const int dtype = options->dtype;
+    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    int dev = 0, sms = 0;
+    st = noalloc_device(&dev, &sms);
+    if (st != GEMM_OK) return st;
+    Plan p;
+    st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, *options, sms, &p);
+    if (st != GEMM_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    switch (p.kind) {
+        case Kind::Nothing: return GEMM_OK;
+        case Kind::ZeroFill: return launch_status(fill_zero_launch(C, M, N, ldc, stream), "fill_zero");
+        case Kind::Generic:
+            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, stream),
+                                 "generic_gemm");
+        case Kind::Sgemm:
+            return launch_status(sgemm_launch(p.sg_bm, p.sg_bn, static_cast<const float*>(A),
+                                              static_cast<const float*>(B), C, M, N, K, lda, ldb,
+                                              ldc, stream),
+                                 "sgemm");
+        case Kind::Tc: {
+            EncodeTiledFn enc = encode_fn();
+            if (!enc) {
+                snprintf(t_last_error, sizeof(t_last_error),
+                         "cuTensorMapEncodeTiled entry point unavailable");
+                return GEMM_ERR_CUDA;
+            }
+            if (p.tc.splits > 1) {
+                const size_t counter_bytes = p.n_counters * sizeof(uint32_t);
+                const size_t ws_bytes = p.ws_floats * sizeof(float);
+                if (counter_bytes > kNoallocCounterBytes ||
+                    ws_bytes > kNoallocScratchBytes - kNoallocCounterBytes) {
+                    snprintf(t_last_error, sizeof(t_last_error),
+                             "split-K scratch of %zu bytes (+%zu counter bytes) exceeds the "
+                             "no-alloc maximum of %zu (+%zu); use fewer K slices or gemm_ex",
+                             ws_bytes, counter_bytes, kNoallocScratchBytes - kNoallocCounterBytes,
+                             kNoallocCounterBytes);
+                    return GEMM_ERR_INVALID_VALUE;
+                }
+                unsigned char* base = nullptr;
+                st = noalloc_scratch(dev, &base);
+                if (st != GEMM_OK) return st;
+                p.tc.counters = reinterpret_cast<uint32_t*>(base);
+                p.tc.ws = reinterpret_cast<float*>(base + kNoallocCounterBytes);
+                // The kernel leaves its counters at zero, but a call that gave up a
+                // wait may not have; start every call from zero.
+                cudaError_t e = cudaMemsetAsync(p.tc.counters, 0, counter_bytes, stream);
+                if (e != cudaSuccess) {
+                    note_cuda_error(e, "cudaMemsetAsync(no-alloc counters)");
+                    return GEMM_ERR_CUDA;
+                }
+            }
+            return launch_status(tc_gemm_launch(p.tc, enc, stream), "tc_gemm");
+        }
+    }
+    return GEMM_ERR_INVALID_VALUE;
+}

@@ -157,6 +157,44 @@ gemm_status_t gemm_device_error(gemm_stream_t stream);
  * device after synchronising the device.  Later calls allocate again. */
 gemm_status_t gemm_release_workspace(void);
 
+/*
+ * gemm_ex_noalloc -- gemm_ex for callers that cannot allocate device memory.
+ * (An addition of this library; the pages have no counterpart.)
+ *
+ * Who needs it: applications that give the GPU's memory to their own pool at
+ * start-up and account for every byte, and latency-critical loops in which a
+ * cudaMalloc or cudaFree -- which can synchronise the whole device -- is not
+ * acceptable.  gemm_ex may allocate its split-K workspace on first use; this
+ * entry point never calls cudaMalloc, cudaFree or any other allocating
+ * routine.  The caller still passes A, B and C.
+ *
+ * Scratch: the split-K tensor-core kernel keeps its partial tiles and arrival
+ * counters in one static device array of GEMM_NOALLOC_SCRATCH_BYTES (8 MiB:
+ * the first 64 KiB hold counters for up to 4096 tiles, the rest holds partial
+ * tiles).  Every GPU that loads the library holds this array until the
+ * process exits.  A plan whose scratch does not fit returns
+ * GEMM_ERR_INVALID_VALUE, and gemm_last_cuda_error() says how much it needed.
+ * Plans without split-K use no scratch at all.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; each call clears the counters it needs (an asynchronous
+ * memset on `stream`) before its kernel runs.  Calls whose kernels overlap on
+ * the GPU -- for example on two streams at once -- race on the array and give
+ * wrong results: serialise them.
+ *
+ * Arguments, options, layout, errors and results are those of gemm_ex.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+gemm_status_t gemm_ex_noalloc(const void *A, const void *B, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              const gemm_options_t *options, gemm_stream_t stream);
+
 /* Text for a status code (static storage). */
 const char *gemm_status_string(gemm_status_t status);
 

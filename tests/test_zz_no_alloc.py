@@ -1,0 +1,108 @@
+"""gemm_ex_noalloc: the entry point for callers that cannot allocate device
+memory (applications that own all GPU memory through their own pool, or
+latency-critical loops where a cudaMalloc/cudaFree, which can synchronise the
+device, is not acceptable).  Its split-K scratch lives in a fixed array inside
+the library, so here it is compared with gemm_ex, which allocates its
+workspace, on the same inputs and plans, twice in a row -- the second call
+reuses the array the first one left behind.
+
+Collected last on purpose (file name), so a run that stops at the first
+failure has run every other test first; it also passes alone in a fresh
+process."""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_gemm_tensor_tcgen05_gb300 import inputs
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # dtype, M, N, K, options (split-K so that the scratch is used)
+    ("f16", 8, 4096, 8192, dict(tile_n=16, swap_ab=1, split_k=4)),
+    ("bf16", 300, 520, 2000, dict(tile_n=128, swap_ab=0, split_k=3)),
+    ("bf16", 64, 1000, 4096, dict(tile_n=64, swap_ab=1, split_k=7)),
+    ("f16", 256, 768, 640, dict()),     # the planner's own choice
+]
+
+
+@pytest.fixture(scope="module")
+def L():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    from dense_gemm_tensor_tcgen05_gb300 import build
+    assert torch.cuda.is_available(), "GPU tests need a GPU"
+    build.build()
+    oracle.build()
+    return g.lib()
+
+
+def _opts(dtype, **kw):
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    o = g.GemmOptions()
+    o.dtype = gu.CODE[dtype]
+    o.swap_ab = -1
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def _call(L, fn, dt, Ad, Bd, M, N, K, opts):
+    import torch
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    o = _opts(dt, **opts)
+    st = getattr(L, fn)(Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, K, N, N,
+                        ctypes.byref(o), stream)
+    assert st == 0, (fn, st, L.gemm_last_cuda_error())
+    assert L.gemm_device_error(stream) == 0
+    return C.cpu().numpy()
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}")
+def test_noalloc_matches_gemm_ex_twice(L, case):
+    dt, M, N, K, opts = case
+    A, B = gu.make_inputs(dt, "uniform", M, N, K, 77)
+    Ad, Bd = gu.to_device(A, dt), gu.to_device(B, dt)
+    ref = _call(L, "gemm_ex", dt, Ad, Bd, M, N, K, opts)
+    amax, bmax = inputs.bits_abs_max(A, dt), inputs.bits_abs_max(B, dt)
+    for _ in range(2):
+        got = _call(L, "gemm_ex_noalloc", dt, Ad, Bd, M, N, K, opts)
+        cmp = oracle.compare(got, ref.astype(np.float64), K, amax, bmax)
+        assert cmp.ok, str(cmp)
+
+
+def test_noalloc_repeat_calls_take_no_device_memory(L):
+    import torch
+    dt, M, N, K, opts = CASES[0]
+    A, B = gu.make_inputs(dt, "uniform", M, N, K, 78)
+    Ad, Bd = gu.to_device(A, dt), gu.to_device(B, dt)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    o = _opts(dt, **opts)
+    args = (Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, K, N, N, ctypes.byref(o), stream)
+    assert L.gemm_ex_noalloc(*args) == 0          # set-up happens on the first call
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        assert L.gemm_ex_noalloc(*args) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+
+
+def test_noalloc_rejects_scratch_beyond_maximum(L):
+    import torch
+    M = N = K = 2048                               # 128 tiles x 8 slices x 128 KiB >> 8 MiB
+    Ad = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    Bd = torch.zeros((K, N), dtype=torch.float16, device="cuda")
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    o = _opts("f16", tile_n=256, swap_ab=0, split_k=8)
+    st = L.gemm_ex_noalloc(Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, K, N, N,
+                           ctypes.byref(o), torch.cuda.current_stream().cuda_stream)
+    assert st == 1
+    assert b"exceeds the no-alloc maximum" in L.gemm_last_cuda_error()
