@@ -22,7 +22,8 @@ import threading
 
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
-    "gemm_ex_noalloc", "gemm_plan_describe", "gemm_device_error", "gemm_release_workspace", "gemm_version",
+    "gemm_ex_noalloc", "gemm_ex_host", "gemm_plan_describe", "gemm_device_error",
+    "gemm_watchdog_selftest", "gemm_release_workspace", "gemm_version",
     "gemm_launch_count", "matmul", "plan", "GemmOptions", "STATUS", "EXPORTED_SYMBOLS",
 ]
 
@@ -45,6 +46,7 @@ EXPORTED_SYMBOLS = (
     "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex", "gemm_plan_describe",
     "gemm_device_error", "gemm_release_workspace", "gemm_status_string",
     "gemm_last_cuda_error", "gemm_version", "gemm_launch_count", "gemm_ex_noalloc",
+    "gemm_ex_host", "gemm_watchdog_selftest",
 )
 
 
@@ -62,7 +64,7 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
                 ("generic", ctypes.c_int32), ("group_m", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("cta_pair", ctypes.c_int32), ("store_mode", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -91,11 +93,16 @@ def lib() -> ctypes.CDLL:
             L.gemm_ex_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                           ctypes.POINTER(GemmOptions), vp]
             L.gemm_ex_noalloc.restype = ctypes.c_int
+            L.gemm_ex_host.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                       ctypes.POINTER(GemmOptions), vp]
+            L.gemm_ex_host.restype = ctypes.c_int
             L.gemm_plan_describe.argtypes = [ctypes.c_int32, vp, vp, vp, i64, i64, i64, i64, i64,
                                              i64, ctypes.POINTER(GemmOptions), ctypes.c_char_p, i64]
             L.gemm_plan_describe.restype = ctypes.c_int
             L.gemm_device_error.argtypes = [vp]
             L.gemm_device_error.restype = ctypes.c_int
+            L.gemm_watchdog_selftest.argtypes = [ctypes.c_int32, vp]
+            L.gemm_watchdog_selftest.restype = ctypes.c_int
             L.gemm_release_workspace.argtypes = []
             L.gemm_release_workspace.restype = ctypes.c_int
             L.gemm_status_string.argtypes = [ctypes.c_int]
@@ -133,10 +140,12 @@ def sgemm_f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int
     _check(lib().sgemm_f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None))
 
 
-def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0) -> GemmOptions:
+def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0,
+             cta_pair=0, store_mode=0) -> GemmOptions:
     o = GemmOptions()
     o.dtype, o.tile_n, o.split_k, o.swap_ab, o.generic, o.group_m = (
         dtype, tile_n, split_k, swap_ab, generic, group_m)
+    o.cta_pair, o.store_mode = cta_pair, store_mode
     return o
 
 
@@ -154,6 +163,14 @@ def gemm_ex_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ld
     _check(lib().gemm_ex_noalloc(A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o), stream or None))
 
 
+def gemm_ex_host(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                 dtype: int, stream: int = 0, **opts) -> None:
+    """The product with A, B and C in (page-locked) host memory; copies and
+    kernels are pipelined over row panels inside the library."""
+    o = _options(dtype, **opts)
+    _check(lib().gemm_ex_host(A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o), stream or None))
+
+
 def gemm_plan_describe(dtype: int, A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
                        ldb: int, ldc: int, **opts) -> str:
     o = _options(dtype, **opts)
@@ -165,6 +182,11 @@ def gemm_plan_describe(dtype: int, A: int, B: int, C: int, M: int, N: int, K: in
 
 def gemm_device_error(stream: int = 0) -> None:
     _check(lib().gemm_device_error(stream or None))
+
+
+def gemm_watchdog_selftest(limit_ms: int = 20, stream: int = 0) -> None:
+    """Enqueue the watchdog self-test kernel (see include/gb300gemm.h)."""
+    _check(lib().gemm_watchdog_selftest(limit_ms, stream or None))
 
 
 def gemm_release_workspace() -> None:
@@ -200,42 +222,46 @@ def _row_major_ld(t, name: str) -> int:
 
 
 def matmul(A, B, out=None, stream=None, **opts):
-    """C = A @ B for 2-D CUDA tensors (row-major, any row stride).
+    """C = A @ B for 2-D tensors (row-major, any row stride).
 
     A and B: both float16, both bfloat16 or both float32; C is float32.
-    Inputs on the CPU are copied to the current device, the product runs
-    there, and the result is copied back into a CPU tensor (the copies are
-    issued on the same stream).  ``opts`` are gemm_options_t fields
-    (tile_n, split_k, swap_ab, generic, group_m) and route through gemm_ex.
+    CUDA tensors run gemm_f16f32 / gemm_bf16f32 / sgemm_f32 (or gemm_ex when
+    plan options are given) on the current (or given) stream and return at
+    once.  CPU tensors go through gemm_ex_host -- the library copies them in,
+    multiplies and copies C back, pipelined over row panels -- and the call
+    returns the CPU result after synchronising the stream (pass page-locked
+    tensors for overlapped copies).  ``opts`` are gemm_options_t fields
+    (tile_n, split_k, swap_ab, generic, group_m, cta_pair).
     """
     import torch
 
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
     code = _code(A)
-    host = not A.is_cuda
-    if host != (not B.is_cuda):
+    if A.is_cuda != B.is_cuda:
         raise ValueError("A and B must both be on the GPU or both on the host")
-    st = stream if stream is not None else torch.cuda.current_stream()
-    if host:
-        with torch.cuda.stream(st):
-            Ad = A.to("cuda", non_blocking=True)
-            Bd = B.to("cuda", non_blocking=True)
-    else:
-        Ad, Bd = A, B
-    M, K = Ad.shape
-    K2, N = Bd.shape
+    M, K = A.shape
+    K2, N = B.shape
     if K != K2:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
-    if out is None or host:
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if not A.is_cuda:
+        if out is None:
+            out = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+        elif out.is_cuda or out.dtype != torch.float32 or tuple(out.shape) != (M, N):
+            raise ValueError("out must be a float32 CPU tensor of shape (M, N)")
+        lda, ldb, ldc = _row_major_ld(A, "A"), _row_major_ld(B, "B"), _row_major_ld(out, "C")
+        gemm_ex_host(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc,
+                     dtype=code, stream=st.cuda_stream, **opts)
+        st.synchronize()
+        return out
+    if out is None:
         with torch.cuda.stream(st):
-            Cd = torch.empty((M, N), dtype=torch.float32, device=Ad.device)
-    else:
-        Cd = out
-        if Cd.dtype != torch.float32 or tuple(Cd.shape) != (M, N):
-            raise ValueError("out must be float32 of shape (M, N)")
-    lda, ldb, ldc = _row_major_ld(Ad, "A"), _row_major_ld(Bd, "B"), _row_major_ld(Cd, "C")
-    args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, lda, ldb, ldc)
+            out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
+        raise ValueError("out must be a float32 CUDA tensor of shape (M, N)")
+    lda, ldb, ldc = _row_major_ld(A, "A"), _row_major_ld(B, "B"), _row_major_ld(out, "C")
+    args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc)
     sh = st.cuda_stream
     if opts:
         gemm_ex(*args, dtype=code, stream=sh, **opts)
@@ -245,13 +271,7 @@ def matmul(A, B, out=None, stream=None, **opts):
         gemm_bf16f32(*args, stream=sh)
     else:
         sgemm_f32(*args, stream=sh)
-    if host:
-        res = out if out is not None else torch.empty((M, N), dtype=torch.float32, pin_memory=True)
-        with torch.cuda.stream(st):
-            res.copy_(Cd, non_blocking=True)
-        st.synchronize()
-        return res
-    return Cd
+    return out
 
 
 def plan(A, B, out=None, **opts) -> str:

@@ -5,6 +5,7 @@
 // stride in elements, C overwritten) are those of the header; see there for
 // the page passages they follow.
 
+#include <algorithm>
 #include <climits>
 #include <cstdio>
 #include <cstring>
@@ -60,6 +61,46 @@ gemm_status_t current_device(int* dev, DeviceInfo* info) {
     *info = d;
     if (d.major != 10 || d.minor != 3) return GEMM_ERR_UNSUPPORTED_DEVICE;
     return GEMM_OK;
+}
+
+// Most CTA-pair clusters (256-wide tiles) resident at once on the current
+// device; 0 if the query fails (the pair kernel is then not planned).
+int pair_clusters() {
+    static std::mutex mu;
+    static int cache[64];
+    static bool known[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!known[dev]) {
+        int n = 0;
+        if (tc_pair_max_clusters(256, &n) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cache[dev] = n;
+        known[dev] = true;
+    }
+    return cache[dev];
+}
+
+// Resident SGEMM CTAs on the whole device for a tile shape (cached per device).
+int sgemm_slots(int bm, int bn, int sms) {
+    static std::mutex mu;
+    static int cache[64][3];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int idx = (bm == 128 && bn == 128) ? 0 : (bm == 128 ? 1 : 2);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev][idx]) {
+        int n = 0;
+        if (sgemm_blocks_per_sm(bm, bn, &n) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev][idx] = n;
+    }
+    return cache[dev][idx] * sms;
 }
 
 EncodeTiledFn encode_fn() {
@@ -171,7 +212,7 @@ enum class Kind { Nothing, ZeroFill, Tc, Generic, Sgemm };
 struct Plan {
     Kind kind = Kind::Nothing;
     TcLaunch tc{};
-    int sg_bm = 0, sg_bn = 0;
+    SgemmLaunch sg{};
     int64_t units = 0;
     size_t ws_floats = 0, n_counters = 0;
 };
@@ -197,17 +238,62 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
             p.kind = Kind::Generic;
         } else {
             p.kind = Kind::Sgemm;
-            const int64_t t128 = ceil_div(M, 128) * ceil_div(N, 128);
-            const int64_t t64 = ceil_div(M, 128) * ceil_div(N, 64);
-            if (o.tile_n == 128 || (o.tile_n == 0 && t128 >= sms)) {
-                p.sg_bm = 128; p.sg_bn = 128;
-            } else if (o.tile_n == 64 || (o.tile_n == 0 && t64 >= sms)) {
-                p.sg_bm = 128; p.sg_bn = 64;
+            SgemmLaunch& S = p.sg;
+            S.A = static_cast<const float*>(A);
+            S.B = static_cast<const float*>(B);
+            S.C = C;
+            S.M = M; S.N = N; S.K = K; S.lda = lda; S.ldb = ldb; S.ldc = ldc;
+            if (o.tile_n == 128 || (o.tile_n == 0 && M > 64 && N > 64)) {
+                S.bm = 128; S.bn = 128;
+            } else if (o.tile_n == 64 || (o.tile_n == 0 && M > 64)) {
+                S.bm = 128; S.bn = 64;
             } else if (o.tile_n == 0 || o.tile_n == 32) {
-                p.sg_bm = 64; p.sg_bn = 64;
+                S.bm = 64; S.bn = 64;
             } else {
                 return GEMM_ERR_INVALID_VALUE;
             }
+            if (o.split_k < 0 || o.split_k > 64) return GEMM_ERR_INVALID_VALUE;
+            const int bk = sgemm_k_step();
+            const int64_t tiles = ceil_div(M, S.bm) * ceil_div(N, S.bn);
+            const int64_t kb = ceil_div(K, bk);
+            const int64_t slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms));
+            auto part = [&](int64_t t0, int64_t nt, int64_t splits) {
+                splits = std::max<int64_t>(1, std::min<int64_t>(splits, kb));
+                const int64_t chunk = ceil_div(ceil_div(K, splits), bk) * bk;
+                splits = ceil_div(K, chunk);   // no empty slices
+                SgemmPart& q = S.parts[S.nparts++];
+                q.tile0 = static_cast<int>(t0);
+                q.tiles = static_cast<int>(nt);
+                q.splits = static_cast<int>(splits);
+                q.k_chunk = static_cast<int>(chunk);
+                if (splits > 1) {
+                    p.ws_floats = std::max<size_t>(p.ws_floats, static_cast<size_t>(nt * splits * S.bm * S.bn));
+                    p.n_counters = std::max<size_t>(p.n_counters, static_cast<size_t>(nt));
+                }
+            };
+            S.nparts = 0;
+            if (o.split_k > 0) {
+                part(0, tiles, o.split_k);
+            } else if (slots > 0 && tiles >= slots) {
+                // Whole waves as they are; a short last wave is split along K so
+                // that it occupies more CTAs for less time.
+                const int64_t waves = tiles / slots;
+                const int64_t tail = tiles - waves * slots;
+                const int64_t s_tail = std::min<int64_t>({4, tail ? slots / tail : 1, kb / 16});
+                if (tail > 0 && 2 * tail <= slots && s_tail >= 2) {
+                    part(0, waves * slots, 1);
+                    part(waves * slots, tail, s_tail);
+                } else {
+                    part(0, tiles, 1);
+                }
+            } else if (slots > 0) {
+                // Fewer tiles than resident CTAs: split K to fill the GPU.
+                part(0, tiles, std::min<int64_t>({8, slots / std::max<int64_t>(tiles, 1), kb / 16}));
+            } else {
+                part(0, tiles, 1);
+            }
+            p.units = 0;
+            for (int i = 0; i < S.nparts; ++i) p.units += static_cast<int64_t>(S.parts[i].tiles) * S.parts[i].splits;
         }
         *plan = p;
         return GEMM_OK;
@@ -226,11 +312,42 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     L.M = M; L.N = N; L.K = K; L.lda = lda; L.ldb = ldb; L.ldc = ldc;
     L.fmt = dtype;
     L.swap = (o.swap_ab < 0) ? ((M <= 64 && N > M) ? 1 : 0) : (o.swap_ab ? 1 : 0);
+    if (o.cta_pair < 0 || o.cta_pair > 2) return GEMM_ERR_INVALID_VALUE;
+    if (o.store_mode < 0 || o.store_mode > 1) return GEMM_ERR_INVALID_VALUE;
+    L.store_mode = o.store_mode;
+
+    // CTA pairs: two SMs share a 256-row tile (each loads half the operand
+    // bytes a 128-row tile would).  Chosen when there is at least a full wave
+    // of such tiles and no split-K is asked for.
+    if (o.cta_pair == 2 || (o.cta_pair == 0 && !L.swap && o.split_k <= 1 && M >= 256 &&
+                            N >= 256 && K >= 512 && (o.tile_n == 0 || o.tile_n == 256))) {
+        const int max_cl = pair_clusters();
+        const int bn = o.tile_n ? o.tile_n : 256;
+        const int64_t units = ceil_div(M, 2 * kTcBM) * ceil_div(N, bn);
+        const bool forced = o.cta_pair == 2;
+        if (forced && (L.swap || o.split_k > 1 || !tc_config_supported(bn, 0, 1) || max_cl < 1))
+            return GEMM_ERR_INVALID_VALUE;
+        if (max_cl >= 1 && (forced || units >= max_cl)) {
+            L.pair = 1;
+            L.bn = bn;
+            L.splits = 1;
+            int64_t group = o.group_m > 0 ? o.group_m : 8;
+            const int64_t tiles_p = ceil_div(M, 2 * kTcBM);
+            if (group > tiles_p) group = tiles_p;
+            L.group = static_cast<int>(group);
+            const int64_t clusters = std::min<int64_t>(units, max_cl);
+            L.grid = static_cast<int>(2 * clusters);
+            p.units = units;
+            p.kind = Kind::Tc;
+            *plan = p;
+            return GEMM_OK;
+        }
+    }
 
     const int64_t pe = L.swap ? N : M;     // extent along the MMA M side
     const int64_t qe = L.swap ? M : N;     // extent along the MMA N side
     if (o.tile_n) {
-        if (!tc_config_supported(o.tile_n, L.swap)) return GEMM_ERR_INVALID_VALUE;
+        if (!tc_config_supported(o.tile_n, L.swap, 0)) return GEMM_ERR_INVALID_VALUE;
         L.bn = o.tile_n;
     } else if (L.swap) {
         L.bn = qe <= 16 ? 16 : qe <= 32 ? 32 : 64;
@@ -298,12 +415,22 @@ void describe(const Plan& p, int dtype, char* buf, int64_t size) {
         case Kind::Nothing: snprintf(buf, n, "nothing (empty output)"); break;
         case Kind::ZeroFill: snprintf(buf, n, "zero-fill (K == 0)"); break;
         case Kind::Generic: snprintf(buf, n, "generic cuda-core dtype=%d tile=64x64", dtype); break;
-        case Kind::Sgemm: snprintf(buf, n, "sgemm tile=%dx%dx8", p.sg_bm, p.sg_bn); break;
+        case Kind::Sgemm: {
+            const SgemmPart& a = p.sg.parts[0];
+            if (p.sg.nparts == 1)
+                snprintf(buf, n, "sgemm tile=%dx%dx%d tiles=%d split_k=%d units=%lld", p.sg.bm,
+                         p.sg.bn, sgemm_k_step(), a.tiles, a.splits, static_cast<long long>(p.units));
+            else
+                snprintf(buf, n, "sgemm tile=%dx%dx%d tiles=%d+%d split_k=%d+%d units=%lld",
+                         p.sg.bm, p.sg.bn, sgemm_k_step(), a.tiles, p.sg.parts[1].tiles, a.splits,
+                         p.sg.parts[1].splits, static_cast<long long>(p.units));
+            break;
+        }
         case Kind::Tc:
             snprintf(buf, n,
-                     "tcgen05 fmt=%s tile=128x%d swap=%d split_k=%d group=%d units=%lld grid=%d",
-                     p.tc.fmt ? "bf16" : "f16", p.tc.bn, p.tc.swap, p.tc.splits, p.tc.group,
-                     static_cast<long long>(p.units), p.tc.grid);
+                     "tcgen05 fmt=%s tile=%dx%d pair=%d swap=%d split_k=%d group=%d units=%lld grid=%d",
+                     p.tc.fmt ? "bf16" : "f16", p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
+                     p.tc.swap, p.tc.splits, p.tc.group, static_cast<long long>(p.units), p.tc.grid);
             break;
     }
 }
@@ -340,10 +467,11 @@ gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, 
             return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
-            return launch_status(sgemm_launch(p.sg_bm, p.sg_bn, static_cast<const float*>(A),
-                                              static_cast<const float*>(B), C, M, N, K, lda, ldb,
-                                              ldc, stream),
-                                 "sgemm");
+            if (p.ws_floats) {
+                st = get_workspace(dev, stream, p.ws_floats, p.n_counters, &p.sg.ws, &p.sg.counters);
+                if (st != GEMM_OK) return st;
+            }
+            return launch_status(sgemm_launch(p.sg, stream), "sgemm");
         case Kind::Tc: {
             EncodeTiledFn enc = encode_fn();
             if (!enc) {
@@ -446,6 +574,17 @@ gemm_status_t gemm_device_error(gemm_stream_t stream) {
         return GEMM_ERR_DEVICE_TIMEOUT;
     }
     return GEMM_OK;
+}
+
+gemm_status_t gemm_watchdog_selftest(int32_t limit_ms, gemm_stream_t stream) {
+    if (limit_ms < 1 || limit_ms > 2000) return GEMM_ERR_INVALID_VALUE;
+    int dev;
+    DeviceInfo info;
+    gemm_status_t st = current_device(&dev, &info);
+    if (st != GEMM_OK) return st;
+    return launch_status(watchdog_selftest_launch(static_cast<uint64_t>(limit_ms) * 1000000ull,
+                                                  reinterpret_cast<cudaStream_t>(stream)),
+                         "watchdog_selftest");
 }
 
 gemm_status_t gemm_release_workspace(void) {
@@ -555,6 +694,36 @@ gemm_status_t noalloc_device(int* dev, int* sms) {
     return GEMM_OK;
 }
 
+// Point a split-K plan at the static scratch: checks the plan's size against
+// the maximum and clears the counters it needs on `stream`.
+gemm_status_t noalloc_bind_scratch(int dev, const Plan& p, cudaStream_t stream, float** ws,
+                                   uint32_t** counters) {
+    const size_t counter_bytes = p.n_counters * sizeof(uint32_t);
+    const size_t ws_bytes = p.ws_floats * sizeof(float);
+    if (counter_bytes > kNoallocCounterBytes ||
+        ws_bytes > kNoallocScratchBytes - kNoallocCounterBytes) {
+        snprintf(t_last_error, sizeof(t_last_error),
+                 "split-K scratch of %zu bytes (+%zu counter bytes) exceeds the "
+                 "no-alloc maximum of %zu (+%zu); use fewer K slices or gemm_ex",
+                 ws_bytes, counter_bytes, kNoallocScratchBytes - kNoallocCounterBytes,
+                 kNoallocCounterBytes);
+        return GEMM_ERR_INVALID_VALUE;
+    }
+    unsigned char* base = nullptr;
+    gemm_status_t st = noalloc_scratch(dev, &base);
+    if (st != GEMM_OK) return st;
+    *counters = reinterpret_cast<uint32_t*>(base);
+    *ws = reinterpret_cast<float*>(base + kNoallocCounterBytes);
+    // The kernels leave their counters at zero, but a call that gave up a
+    // wait may not have; start every call from zero.
+    cudaError_t e = cudaMemsetAsync(*counters, 0, counter_bytes, stream);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaMemsetAsync(no-alloc counters)");
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C, int64_t M,
@@ -581,10 +750,11 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
             return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
-            return launch_status(sgemm_launch(p.sg_bm, p.sg_bn, static_cast<const float*>(A),
-                                              static_cast<const float*>(B), C, M, N, K, lda, ldb,
-                                              ldc, stream),
-                                 "sgemm");
+            if (p.ws_floats) {
+                st = noalloc_bind_scratch(dev, p, stream, &p.sg.ws, &p.sg.counters);
+                if (st != GEMM_OK) return st;
+            }
+            return launch_status(sgemm_launch(p.sg, stream), "sgemm");
         case Kind::Tc: {
             EncodeTiledFn enc = encode_fn();
             if (!enc) {
@@ -593,32 +763,182 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
                 return GEMM_ERR_CUDA;
             }
             if (p.tc.splits > 1) {
-                const size_t counter_bytes = p.n_counters * sizeof(uint32_t);
-                const size_t ws_bytes = p.ws_floats * sizeof(float);
-                if (counter_bytes > kNoallocCounterBytes ||
-                    ws_bytes > kNoallocScratchBytes - kNoallocCounterBytes) {
-                    snprintf(t_last_error, sizeof(t_last_error),
-                             "split-K scratch of %zu bytes (+%zu counter bytes) exceeds the "
-                             "no-alloc maximum of %zu (+%zu); use fewer K slices or gemm_ex",
-                             ws_bytes, counter_bytes, kNoallocScratchBytes - kNoallocCounterBytes,
-                             kNoallocCounterBytes);
-                    return GEMM_ERR_INVALID_VALUE;
-                }
-                unsigned char* base = nullptr;
-                st = noalloc_scratch(dev, &base);
+                st = noalloc_bind_scratch(dev, p, stream, &p.tc.ws, &p.tc.counters);
                 if (st != GEMM_OK) return st;
-                p.tc.counters = reinterpret_cast<uint32_t*>(base);
-                p.tc.ws = reinterpret_cast<float*>(base + kNoallocCounterBytes);
-                // The kernel leaves its counters at zero, but a call that gave up a
-                // wait may not have; start every call from zero.
-                cudaError_t e = cudaMemsetAsync(p.tc.counters, 0, counter_bytes, stream);
-                if (e != cudaSuccess) {
-                    note_cuda_error(e, "cudaMemsetAsync(no-alloc counters)");
-                    return GEMM_ERR_CUDA;
-                }
             }
             return launch_status(tc_gemm_launch(p.tc, enc, stream), "tc_gemm");
         }
     }
     return GEMM_ERR_INVALID_VALUE;
+}
+
+// ---- host-buffer entry point -------------------------------------------------------
+//
+// gemm_ex_host: A, B and C in host memory.  B is copied to the device once;
+// then M is cut into row panels and, per panel, the A rows go in, the product
+// runs, and the C rows come back -- on three streams (copy in, compute = the
+// caller's stream, copy out) with two device buffers per panel operand, so
+// the copies of one panel overlap the product of the next.  Device staging
+// buffers, the two copy streams and the events are owned by the library, one
+// set per (device, caller stream), allocated on first use and grown as needed.
+
+namespace {
+
+struct HostPipe {
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t e_start = nullptr;
+    cudaEvent_t e_in[2] = {}, e_comp[2] = {}, e_out[2] = {};
+    void* dB = nullptr;
+    size_t dB_bytes = 0;
+    void* dA[2] = {};
+    size_t dA_bytes = 0;
+    void* dC[2] = {};
+    size_t dC_bytes = 0;
+};
+
+std::mutex g_hp_mu;
+std::map<std::pair<int, cudaStream_t>, HostPipe> g_hp;
+
+gemm_status_t grow(void** p, size_t* have, size_t want, const char* what) {
+    if (*have >= want) return GEMM_OK;
+    if (*p) {
+        cudaFree(*p);
+        *p = nullptr;
+        *have = 0;
+    }
+    cudaError_t e = cudaMalloc(p, want);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, what);
+        *p = nullptr;
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
+    *have = want;
+    return GEMM_OK;
+}
+
+gemm_status_t host_pipe(int dev, cudaStream_t stream, size_t b_bytes, size_t a_bytes,
+                        size_t c_bytes, HostPipe** out) {
+    HostPipe& h = g_hp[{dev, stream}];
+    cudaError_t e = cudaSuccess;
+    if (!h.s_in) {
+        if ((e = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h.e_start, cudaEventDisableTiming)) != cudaSuccess) {
+            note_cuda_error(e, "host pipeline streams");
+            return GEMM_ERR_CUDA;
+        }
+        for (int i = 0; i < 2; ++i) {
+            if ((e = cudaEventCreateWithFlags(&h.e_in[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&h.e_comp[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&h.e_out[i], cudaEventDisableTiming)) != cudaSuccess) {
+                note_cuda_error(e, "host pipeline events");
+                return GEMM_ERR_CUDA;
+            }
+        }
+    }
+    if (h.dB_bytes < b_bytes || h.dA_bytes < a_bytes || h.dC_bytes < c_bytes) {
+        // buffers may still be in use by an earlier call on this stream
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) {
+            note_cuda_error(e, "cudaStreamSynchronize");
+            return GEMM_ERR_CUDA;
+        }
+    }
+    gemm_status_t st;
+    if ((st = grow(&h.dB, &h.dB_bytes, b_bytes, "cudaMalloc(host pipeline B)")) != GEMM_OK) return st;
+    for (int i = 0; i < 2; ++i) {
+        // both panel buffers of an operand always have the same size
+        size_t ha = h.dA_bytes, hc = h.dC_bytes;
+        if ((st = grow(&h.dA[i], &ha, a_bytes, "cudaMalloc(host pipeline A)")) != GEMM_OK) return st;
+        if ((st = grow(&h.dC[i], &hc, c_bytes, "cudaMalloc(host pipeline C)")) != GEMM_OK) return st;
+    }
+    h.dA_bytes = std::max(h.dA_bytes, a_bytes);
+    h.dC_bytes = std::max(h.dC_bytes, c_bytes);
+    *out = &h;
+    return GEMM_OK;
+}
+
+// Rows per panel: enough that each panel's product still fills the GPU with
+// several waves of tiles, at most four panels' worth of overlap to win.
+int64_t panel_rows(int64_t M) {
+    if (M <= 1024) return M;
+    int64_t rows = ceil_div(ceil_div(M, 4), 256) * 256;
+    return rows < 512 ? 512 : rows;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                      const gemm_options_t* options, gemm_stream_t stream_handle) {
+    if (!options) return GEMM_ERR_INVALID_VALUE;
+    const int dtype = options->dtype;
+    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
+    const size_t es = dtype == 2 ? 4 : 2;
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es));
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    int dev;
+    DeviceInfo info;
+    st = current_device(&dev, &info);
+    if (st != GEMM_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+
+    const int64_t prow = panel_rows(M);
+    const int64_t npanels = ceil_div(M, prow);
+    // device layouts are dense: ld = K for A panels, N for B and C panels
+    const size_t b_bytes = static_cast<size_t>(std::max<int64_t>(K, 1) * N) * es;
+    const size_t a_bytes = static_cast<size_t>(prow * std::max<int64_t>(K, 1)) * es;
+    const size_t c_bytes = static_cast<size_t>(prow * N) * 4;
+
+    std::lock_guard<std::mutex> lk(g_hp_mu);
+    HostPipe* h = nullptr;
+    st = host_pipe(dev, stream, b_bytes, a_bytes, c_bytes, &h);
+    if (st != GEMM_OK) return st;
+
+    cudaError_t e = cudaSuccess;
+#define HP_CHECK(call, what)              \
+    do {                                  \
+        if ((e = (call)) != cudaSuccess) { \
+            note_cuda_error(e, what);     \
+            return GEMM_ERR_CUDA;         \
+        }                                 \
+    } while (0)
+
+    // everything earlier on `stream` (including a previous call's use of the
+    // staging buffers) happens before this call's copies
+    HP_CHECK(cudaEventRecord(h->e_start, stream), "cudaEventRecord");
+    HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_start, 0), "cudaStreamWaitEvent");
+    HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_start, 0), "cudaStreamWaitEvent");
+    if (K > 0)
+        HP_CHECK(cudaMemcpy2DAsync(h->dB, N * es, B, ldb * es, N * es, K, cudaMemcpyHostToDevice,
+                                   h->s_in),
+                 "cudaMemcpy2DAsync(B)");
+    for (int64_t i = 0; i < npanels; ++i) {
+        const int buf = static_cast<int>(i & 1);
+        const int64_t r0 = i * prow;
+        const int64_t rows = std::min<int64_t>(prow, M - r0);
+        if (i >= 2) HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_comp[buf], 0), "cudaStreamWaitEvent");
+        if (K > 0)
+            HP_CHECK(cudaMemcpy2DAsync(h->dA[buf], K * es, static_cast<const char*>(A) + r0 * lda * es,
+                                       lda * es, K * es, rows, cudaMemcpyHostToDevice, h->s_in),
+                     "cudaMemcpy2DAsync(A panel)");
+        HP_CHECK(cudaEventRecord(h->e_in[buf], h->s_in), "cudaEventRecord");
+        HP_CHECK(cudaStreamWaitEvent(stream, h->e_in[buf], 0), "cudaStreamWaitEvent");
+        if (i >= 2) HP_CHECK(cudaStreamWaitEvent(stream, h->e_out[buf], 0), "cudaStreamWaitEvent");
+        st = run(dtype, h->dA[buf], h->dB, static_cast<float*>(h->dC[buf]), rows, N, K, K, N, N,
+                 *options, stream);
+        if (st != GEMM_OK) return st;
+        HP_CHECK(cudaEventRecord(h->e_comp[buf], stream), "cudaEventRecord");
+        HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_comp[buf], 0), "cudaStreamWaitEvent");
+        HP_CHECK(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, h->dC[buf], N * 4, N * 4, rows,
+                                   cudaMemcpyDeviceToHost, h->s_out),
+                 "cudaMemcpy2DAsync(C panel)");
+        HP_CHECK(cudaEventRecord(h->e_out[buf], h->s_out), "cudaEventRecord");
+    }
+    // later work on `stream` (and the caller's synchronisation) sees C
+    const int last = static_cast<int>((npanels - 1) & 1);
+    HP_CHECK(cudaStreamWaitEvent(stream, h->e_out[last], 0), "cudaStreamWaitEvent");
+    if (npanels >= 2) HP_CHECK(cudaStreamWaitEvent(stream, h->e_out[last ^ 1], 0), "cudaStreamWaitEvent");
+#undef HP_CHECK
+    return GEMM_OK;
 }

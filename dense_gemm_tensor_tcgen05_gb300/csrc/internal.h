@@ -22,6 +22,8 @@ struct TcLaunch {
     int fmt;        // 0 = FP16, 1 = BF16
     int bn;         // tile width along the MMA N side
     int swap;       // 1: MMA M side runs along N of C (C^T = B^T A^T)
+    int pair;       // 1: CTA-pair kernel (clusters of 2, 256 x bn tiles)
+    int store_mode;    // 0: TMA stores when C allows them, 1: plain stores
     int splits;     // K slices
     int group;      // raster group height in tiles along the MMA M side
     int grid;       // CTAs (persistent); <= units
@@ -35,22 +37,51 @@ constexpr int kTcBK = 64;   // k per pipeline stage (64 16-bit elements = 128 by
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Which (bn, swap) kernels exist.
-bool tc_config_supported(int bn, int swap);
+// Which (bn, swap, pair) kernels exist.
+bool tc_config_supported(int bn, int swap, int pair);
+
+// Most clusters of the CTA-pair kernel with tile width bn that can be resident
+// at once on the current device.
+cudaError_t tc_pair_max_clusters(int bn, int* n);
 
 // Launch the tensor-core kernel.  Returns the first CUDA error (tensor-map
 // encoding failures are reported as cudaErrorInvalidValue).
 cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t stream);
 
+// Launch the watchdog self-test kernel (a wait nothing satisfies, given up
+// after limit_ns).
+cudaError_t watchdog_selftest_launch(uint64_t limit_ns, cudaStream_t stream);
+
 // Device address of this device's error word (cudaGetSymbolAddress on the
 // tensor-core translation unit's __device__ variable).
 cudaError_t tc_error_word(uint32_t** ptr);
 
-// CUDA-core kernels.
+// CUDA-core SGEMM: up to two launches over row-major linear tile ranges,
+// each with its own K split (the second one spreads the last partial wave of
+// tiles over more CTAs).
+struct SgemmPart {
+    int tile0;      // first linear tile
+    int tiles;      // tiles in this launch
+    int splits;     // K slices per tile
+    int k_chunk;    // K per slice (multiple of the kernel's K step)
+};
+
+struct SgemmLaunch {
+    const float* A;
+    const float* B;
+    float* C;
+    int64_t M, N, K, lda, ldb, ldc;
+    int bm, bn;
+    int nparts;
+    SgemmPart parts[2];
+    float* ws;          // >= max over parts of tiles * splits * bm * bn floats (if any splits > 1)
+    uint32_t* counters; // >= max over parts of tiles, zero between launches
+};
+
 bool sgemm_tile_supported(int bm, int bn);
-cudaError_t sgemm_launch(int bm, int bn, const float* A, const float* B, float* C, int64_t M,
-                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                         cudaStream_t stream);
+cudaError_t sgemm_blocks_per_sm(int bm, int bn, int* n);
+int sgemm_k_step();
+cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                            cudaStream_t stream);

@@ -47,10 +47,26 @@ struct SgemmCfg {
     static_assert(2 * (BK * kAStride + BK * BN) * 4 <= 48 * 1024, "static shared memory");
 };
 
+struct SgArgs {
+    const float* A;
+    const float* B;
+    float* C;
+    int M, N, K;
+    int64_t lda, ldb, ldc;
+    int tiles_n;        // tiles along N
+    int tile0;          // first (row-major linear) tile of this launch
+    int splits;         // K slices per tile; 1 = the whole K
+    int k_chunk;        // K per slice, a multiple of BK
+    float* ws;          // split-K partial tiles of this launch
+    uint32_t* counters; // split-K arrival counter per tile, zero between launches
+};
+
+// Load one BK slice of A (BM x BK) and B (BK x BN) starting at k0 into
+// registers.  Elements at k >= kend, or outside M / N in an edge tile, read
+// as zero.
 template <int BM, int BN, int BK, bool EDGE>
-__device__ __forceinline__ void sgemm_load(const float* __restrict__ A, const float* __restrict__ B,
-                                           int M, int N, int K, int64_t lda, int64_t ldb,
-                                           int m0, int n0, int k0, bool guard_k,
+__device__ __forceinline__ void sgemm_load(const SgArgs& a, int m0, int n0, int k0, int kend,
+                                           bool guard_k,
                                            float4 (&ra)[SgemmCfg<BM, BN, BK>::kAPer],
                                            float4 (&rb)[SgemmCfg<BM, BN, BK>::kBPer]) {
     using Cfg = SgemmCfg<BM, BN, BK>;
@@ -61,15 +77,15 @@ __device__ __forceinline__ void sgemm_load(const float* __restrict__ A, const fl
         const int r = idx / (BK / 4);
         const int kq = (idx % (BK / 4)) * 4;
         const int gm = m0 + r, gk = k0 + kq;
-        const float* src = A + static_cast<int64_t>(gm) * lda + gk;
+        const float* src = a.A + static_cast<int64_t>(gm) * a.lda + gk;
         if (!EDGE && !guard_k) {
             ra[l] = __ldg(reinterpret_cast<const float4*>(src));
-        } else if (gm < M && gk + 3 < K) {
+        } else if (gm < a.M && gk + 3 < kend) {
             ra[l] = __ldg(reinterpret_cast<const float4*>(src));
         } else {
             float t[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) t[i] = (gm < M && gk + i < K) ? __ldg(src + i) : 0.0f;
+            for (int i = 0; i < 4; ++i) t[i] = (gm < a.M && gk + i < kend) ? __ldg(src + i) : 0.0f;
             ra[l] = make_float4(t[0], t[1], t[2], t[3]);
         }
     }
@@ -79,15 +95,15 @@ __device__ __forceinline__ void sgemm_load(const float* __restrict__ A, const fl
         const int kr = idx / (BN / 4);
         const int nq = (idx % (BN / 4)) * 4;
         const int gk = k0 + kr, gn = n0 + nq;
-        const float* src = B + static_cast<int64_t>(gk) * ldb + gn;
+        const float* src = a.B + static_cast<int64_t>(gk) * a.ldb + gn;
         if (!EDGE && !guard_k) {
             rb[l] = __ldg(reinterpret_cast<const float4*>(src));
-        } else if (gk < K && gn + 3 < N) {
+        } else if (gk < kend && gn + 3 < a.N) {
             rb[l] = __ldg(reinterpret_cast<const float4*>(src));
         } else {
             float t[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) t[i] = (gk < K && gn + i < N) ? __ldg(src + i) : 0.0f;
+            for (int i = 0; i < 4; ++i) t[i] = (gk < kend && gn + i < a.N) ? __ldg(src + i) : 0.0f;
             rb[l] = make_float4(t[0], t[1], t[2], t[3]);
         }
     }
@@ -118,47 +134,40 @@ __device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs,
     }
 }
 
+// acc (this thread's 8 x 8 outputs) += A[m0.., kbeg..kend) x B[kbeg..kend, n0..)
 template <int BM, int BN, int BK, bool EDGE>
-__device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const float* __restrict__ B,
-                                           float* __restrict__ C, int M, int N, int K,
-                                           int64_t lda, int64_t ldb, int64_t ldc, int m0, int n0,
-                                           float* As0, float* Bs0) {
+__device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, int kbeg, int kend,
+                                               float* As0, float* Bs0, float (&acc)[8][8]) {
     using Cfg = SgemmCfg<BM, BN, BK>;
     const int tx = threadIdx.x % Cfg::kTx;
     const int ty = threadIdx.x / Cfg::kTx;
-    const int k_tiles = (K + BK - 1) / BK;
-    const int k_full = K / BK;   // slices with no K tail
-
-    float acc[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    const int k_tiles = (kend - kbeg + BK - 1) / BK;
+    const int k_full = (kend - kbeg) / BK;   // slices with no K tail
 
     float4 ra[Cfg::kAPer], rb[Cfg::kBPer];
-    sgemm_load<BM, BN, BK, EDGE>(A, B, M, N, K, lda, ldb, m0, n0, 0, 0 >= k_full, ra, rb);
+    sgemm_load<BM, BN, BK, EDGE>(a, m0, n0, kbeg, kend, 0 >= k_full, ra, rb);
     sgemm_store_smem<BM, BN, BK>(As0, Bs0, ra, rb);
     __syncthreads();
 
     for (int kt = 0; kt < k_tiles; ++kt) {
-        float* As = As0 + (kt & 1) * (BK * Cfg::kAStride);
-        float* Bs = Bs0 + (kt & 1) * (BK * BN);
+        const float* As = As0 + (kt & 1) * (BK * Cfg::kAStride);
+        const float* Bs = Bs0 + (kt & 1) * (BK * BN);
         const bool more = kt + 1 < k_tiles;
         if (more)
-            sgemm_load<BM, BN, BK, EDGE>(A, B, M, N, K, lda, ldb, m0, n0, (kt + 1) * BK,
-                                         kt + 1 >= k_full, ra, rb);
+            sgemm_load<BM, BN, BK, EDGE>(a, m0, n0, kbeg + (kt + 1) * BK, kend, kt + 1 >= k_full,
+                                         ra, rb);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + ty * 4);
             const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + BM / 2 + ty * 4);
             const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * BN + tx * 4);
             const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * BN + BN / 2 + tx * 4);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
         if (more) {
             float* An = As0 + ((kt + 1) & 1) * (BK * Cfg::kAStride);
@@ -167,15 +176,23 @@ __device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const fl
         }
         __syncthreads();
     }
+}
 
-    // store: quadrant (qi, qj) rows m0 + qi*BM/2 + ty*4 + i, columns n0 + qj*BN/2 + tx*4 + j
+// Quadrant (qi, qj) of the micro-tile: rows m0 + qi*BM/2 + ty*4 + i,
+// columns n0 + qj*BN/2 + tx*4 + j.
+template <int BM, int BN, int BK, bool EDGE>
+__device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
+                                              const float (&acc)[8][8]) {
+    using Cfg = SgemmCfg<BM, BN, BK>;
+    const int tx = threadIdx.x % Cfg::kTx;
+    const int ty = threadIdx.x / Cfg::kTx;
 #pragma unroll
     for (int qi = 0; qi < 2; ++qi) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int gm = m0 + qi * (BM / 2) + ty * 4 + i;
-            if (EDGE && gm >= M) continue;
-            float* crow = C + static_cast<int64_t>(gm) * ldc;
+            if (EDGE && gm >= a.M) continue;
+            float* crow = a.C + static_cast<int64_t>(gm) * a.ldc;
 #pragma unroll
             for (int qj = 0; qj < 2; ++qj) {
                 const int gn = n0 + qj * (BN / 2) + tx * 4;
@@ -185,35 +202,120 @@ __device__ __forceinline__ void sgemm_tile(const float* __restrict__ A, const fl
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (gn + j < N) crow[gn + j] = v[j];
+                        if (gn + j < a.N) crow[gn + j] = v[j];
                 }
             }
         }
     }
 }
 
+// One CTA per (tile, K slice).  With one slice the tile goes straight to C.
+// With several, each slice stores its partial tile to the workspace and the
+// CTA that finishes last sums the partials in slice order 0..S-1 (fixed
+// order: the result does not depend on timing) and writes C.
 template <int BM, int BN, int BK>
-__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK>::kThreads)
-sgemm_kernel(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
-             int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc) {
+__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK>::kThreads, (BM * BN >= 128 * 128) ? 2 : 1)
+sgemm_kernel(const SgArgs a) {
     using Cfg = SgemmCfg<BM, BN, BK>;
     __shared__ __align__(16) float As[2 * BK * Cfg::kAStride];
     __shared__ __align__(16) float Bs[2 * BK * BN];
-    const int m0 = blockIdx.y * BM;
-    const int n0 = blockIdx.x * BN;
-    if (m0 + BM <= M && n0 + BN <= N)
-        sgemm_tile<BM, BN, BK, false>(A, B, C, M, N, K, lda, ldb, ldc, m0, n0, As, Bs);
+    __shared__ uint32_t s_last;
+    const int u = blockIdx.x;
+    const int t = a.tile0 + u / a.splits;
+    const int slice = u - (u / a.splits) * a.splits;
+    const int m0 = (t / a.tiles_n) * BM;
+    const int n0 = (t - (t / a.tiles_n) * a.tiles_n) * BN;
+    const int kbeg = slice * a.k_chunk;
+    const int kend = min(a.K, kbeg + a.k_chunk);
+    const bool edge = !(m0 + BM <= a.M && n0 + BN <= a.N);
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    if (!edge)
+        sgemm_mainloop<BM, BN, BK, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
     else
-        sgemm_tile<BM, BN, BK, true>(A, B, C, M, N, K, lda, ldb, ldc, m0, n0, As, Bs);
+        sgemm_mainloop<BM, BN, BK, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
+
+    if (a.splits == 1) {
+        if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
+        else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+        return;
+    }
+
+    // partial tile: this thread's 16 float4, interleaved across threads so a
+    // warp's stores are contiguous
+    const int tid = threadIdx.x;
+    const int local_tile = u / a.splits;
+    float4* slot = reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(u) * (BM * BN));
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        slot[q * Cfg::kThreads + tid] = make_float4(acc[q >> 1][(q & 1) * 4], acc[q >> 1][(q & 1) * 4 + 1],
+                                                    acc[q >> 1][(q & 1) * 4 + 2], acc[q >> 1][(q & 1) * 4 + 3]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(a.counters + local_tile, 1u);
+        s_last = (old == static_cast<uint32_t>(a.splits - 1)) ? 1u : 0u;
+        if (s_last) atomicExch(a.counters + local_tile, 0u);   // ready for the next launch
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int s2 = 0; s2 < a.splits; ++s2) {
+        const float4* src = reinterpret_cast<const float4*>(
+            a.ws + (static_cast<int64_t>(local_tile) * a.splits + s2) * (BM * BN));
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 v = __ldcg(src + q * Cfg::kThreads + tid);
+            acc[q >> 1][(q & 1) * 4] += v.x;
+            acc[q >> 1][(q & 1) * 4 + 1] += v.y;
+            acc[q >> 1][(q & 1) * 4 + 2] += v.z;
+            acc[q >> 1][(q & 1) * 4 + 3] += v.w;
+        }
+    }
+    if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
+    else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
 }
 
-template <int BM, int BN, int BK>
-static cudaError_t sgemm_go(const float* A, const float* B, float* C, int64_t M, int64_t N,
-                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream) {
-    dim3 grid(static_cast<unsigned>(ceil_div(N, BN)), static_cast<unsigned>(ceil_div(M, BM)));
-    sgemm_kernel<BM, BN, BK><<<grid, SgemmCfg<BM, BN, BK>::kThreads, 0, stream>>>(
-        A, B, C, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), lda, ldb, ldc);
-    return cudaGetLastError();
+#ifndef GB300_SGEMM_BK
+#define GB300_SGEMM_BK 16
+#endif
+constexpr int kSgemmBK = GB300_SGEMM_BK;
+
+template <int BM, int BN>
+static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
+    for (int i = 0; i < L.nparts; ++i) {
+        const SgemmPart& part = L.parts[i];
+        SgArgs a;
+        a.A = L.A;
+        a.B = L.B;
+        a.C = L.C;
+        a.M = static_cast<int>(L.M);
+        a.N = static_cast<int>(L.N);
+        a.K = static_cast<int>(L.K);
+        a.lda = L.lda;
+        a.ldb = L.ldb;
+        a.ldc = L.ldc;
+        a.tiles_n = static_cast<int>(ceil_div(L.N, BN));
+        a.tile0 = part.tile0;
+        a.splits = part.splits;
+        a.k_chunk = part.k_chunk;
+        a.ws = L.ws;
+        a.counters = L.counters;
+        sgemm_kernel<BM, BN, kSgemmBK>
+            <<<static_cast<unsigned>(part.tiles) * part.splits, SgemmCfg<BM, BN, kSgemmBK>::kThreads, 0,
+               stream>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // ------------------------------------------------------------- generic --
@@ -290,12 +392,25 @@ bool sgemm_tile_supported(int bm, int bn) {
     return (bm == 128 && bn == 128) || (bm == 128 && bn == 64) || (bm == 64 && bn == 64);
 }
 
-cudaError_t sgemm_launch(int bm, int bn, const float* A, const float* B, float* C, int64_t M,
-                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                         cudaStream_t stream) {
-    if (bm == 128 && bn == 128) return sgemm_go<128, 128, 8>(A, B, C, M, N, K, lda, ldb, ldc, stream);
-    if (bm == 128 && bn == 64) return sgemm_go<128, 64, 8>(A, B, C, M, N, K, lda, ldb, ldc, stream);
-    if (bm == 64 && bn == 64) return sgemm_go<64, 64, 8>(A, B, C, M, N, K, lda, ldb, ldc, stream);
+cudaError_t sgemm_blocks_per_sm(int bm, int bn, int* n) {
+    if (bm == 128 && bn == 128)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            n, sgemm_kernel<128, 128, kSgemmBK>, SgemmCfg<128, 128, kSgemmBK>::kThreads, 0);
+    if (bm == 128 && bn == 64)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            n, sgemm_kernel<128, 64, kSgemmBK>, SgemmCfg<128, 64, kSgemmBK>::kThreads, 0);
+    if (bm == 64 && bn == 64)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            n, sgemm_kernel<64, 64, kSgemmBK>, SgemmCfg<64, 64, kSgemmBK>::kThreads, 0);
+    return cudaErrorInvalidValue;
+}
+
+int sgemm_k_step() { return kSgemmBK; }
+
+cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream) {
+    if (L.bm == 128 && L.bn == 128) return sgemm_go<128, 128>(L, stream);
+    if (L.bm == 128 && L.bn == 64) return sgemm_go<128, 64>(L, stream);
+    if (L.bm == 64 && L.bn == 64) return sgemm_go<64, 64>(L, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -43,6 +43,7 @@
 // its own MMAs, and tensor memory is freed on every path.
 
 #include <cstdio>
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -51,11 +52,13 @@ namespace gb300 {
 
 __device__ uint32_t g_tc_error;  // device error word; bits below
 
-constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u;
+constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u,
+                   kErrSelfTest = 16u;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s for copies already in flight
 constexpr int kThreads = 192;
 constexpr int kUmmaK = 16;
+constexpr int kStoreStageBytes = 4 * 2 * 4096;   // epilogue staging: 4 warps x two 4 KiB buffers
 
 struct TcArgs {
     float* C;
@@ -66,6 +69,7 @@ struct TcArgs {
     int32_t splits, kb_total, kb_per_split;
     int32_t group;
     int32_t vec_store;          // C rows are 16-byte aligned: float4 stores allowed
+    int32_t tma_store;          // epilogue writes C through the TMA store map
     uint32_t idesc;
     float* ws;
     uint32_t* counters;
@@ -80,8 +84,9 @@ struct TcTraits {
                                  : (BN == 32) ? 9 : 10;
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;  // two accumulators
     static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kStoreBytes = SWAP ? 0 : kStoreStageBytes;   // epilogue staging
     static constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
-                                      kNumBars * 8 + 16;
+                                      kStoreBytes + kNumBars * 8 + 16;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(SWAP ? (BN <= 64) : (BN >= 64 && BN % 64 == 0), "operand box shapes");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "tensor memory");
@@ -97,13 +102,13 @@ struct WaitCtx {
 // Bounded wait: true when the phase of the given parity completed; false when
 // the CTA is aborting (this wait gave up, or another role did).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                           uint32_t err_bit) {
+                                           uint32_t err_bit, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *w.abort_flag = 1;
             atomicOr(&g_tc_error, err_bit);
             return false;
@@ -172,12 +177,51 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, const float (&v)[W]
     }
 }
 
+// ---- TMA-store epilogue ------------------------------------------------------
+//
+// A warp's 32 accumulator rows x 32 columns (one chunk) go through a 4 KiB
+// staging buffer in shared memory, written in the 128-byte swizzled order the
+// store map expects (16-byte piece j of row r at piece j ^ (r % 8), which
+// also keeps the warp's shared stores free of bank conflicts), and leave with
+// one tensor store.  The TMA unit clips the box to C's bounds, so ragged
+// tiles need no masks.  Each epilogue warp owns two buffers and alternates.
+
+struct StoreStage {
+    uint32_t base;   // this warp's two buffers, 1024-byte aligned
+    int next;
+};
+
+__device__ __forceinline__ void stage_and_store(StoreStage& st, const CUtensorMap* map_c,
+                                                const float (&v)[32], int lane, int col0, int row0,
+                                                int M, int N) {
+    const uint32_t buf = st.base + static_cast<uint32_t>(st.next) * 4096u;
+    if (lane == 0) bulk_wait_group_read<1>();   // the store issued from this buffer has read it
+    __syncwarp();
+    const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(rowaddr + (static_cast<uint32_t>(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
+                     v[4 * j + 2], v[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    // A box wholly past C's end is skipped, and then the same buffer is used
+    // again next time: only buffers that a store was issued from alternate, so
+    // "at most one group still reading" always means the other buffer.
+    if (row0 < M && col0 < N) {
+        if (lane == 0) {
+            tma_store_2d(map_c, buf, col0, row0);
+            bulk_commit_group();
+        }
+        st.next ^= 1;
+    }
+}
+
 // ---- the kernel ---------------------------------------------------------------
 
 template <int BN, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q,
-               const TcArgs args) {
+               const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
     using T = TcTraits<BN, SWAP>;
     constexpr int S = T::kStages;
     constexpr int CW = BN < 32 ? BN : 32;   // accumulator columns per tensor-memory load
@@ -186,7 +230,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t smem_base = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * T::kStageBytes);
+    const uint32_t store_base = smem_base + S * T::kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * T::kStageBytes + T::kStoreBytes);
     const uint32_t bar_base = smem_u32(bars);
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (S + s); };
@@ -215,6 +260,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_p);
         tma_prefetch_map(&map_q);
+        if (!SWAP && args.tma_store) tma_prefetch_map(&map_c);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), T::kTmemCols);
@@ -328,6 +374,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
         // ------------------------------ epilogue ----------------------------------
         const int quarter = warp & 3;                 // tensor-memory lanes 32*quarter ..
         const int row = quarter * 32 + lane;          // lane within the 128-row tile
+        StoreStage stg{store_base + static_cast<uint32_t>(warp - 2) * 8192u, 0};
+        const bool tma_out = !SWAP && args.tma_store;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
@@ -362,6 +410,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
 #pragma unroll
                 for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
                 if (args.splits == 1) {
+                    if constexpr (!SWAP) {
+                        if (tma_out) {
+                            stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
+                                            pb * kTcBM + quarter * 32, args.M, args.N);
+                            continue;
+                        }
+                    }
                     store_chunk<SWAP, CW>(args, v, p, q0 + c * CW);
                 } else {
                     // partial tile, laid out [column][row] so a warp's stores are
@@ -393,6 +448,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
 #pragma unroll
                             for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
                         }
+                        if constexpr (!SWAP) {
+                            if (tma_out) {
+                                stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
+                                                pb * kTcBM + quarter * 32, args.M, args.N);
+                                continue;
+                            }
+                        }
                         store_chunk<SWAP, CW>(args, v, p, q0 + c * CW);
                     }
                 }
@@ -400,6 +462,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (tma_out && lane == 0) bulk_wait_group<0>();   // every tensor store has completed
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -410,11 +474,352 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
     }
 }
 
+// ---- the CTA-pair kernel ---------------------------------------------------------
+//
+// Same roles, pipeline and epilogue as tc_gemm_kernel, for a cluster of two
+// CTAs that share one 256 x BN output tile.  Each CTA loads its own 128 rows
+// of A and its own BN/2 columns of B per stage (so each SM moves two thirds
+// of the bytes a 128 x BN tile needs), and the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256), which reads both CTAs' shared memory
+// and leaves each CTA's 128 rows of D in that CTA's tensor memory.
+//   * both CTAs' TMA copies complete on the even CTA's "full" barrier, which
+//     the even CTA arms for the bytes of both;
+//   * the MMA commits are multicast to both CTAs' "empty", "acc_full" and
+//     drain barriers;
+//   * both CTAs' epilogue warps arrive on the even CTA's "acc_empty" (8
+//     arrivals);
+//   * a CTA that gives up a wait also raises the peer's abort flag, and a
+//     cluster barrier keeps either CTA from freeing tensor memory or exiting
+//     while the pair's MMAs may still read its shared memory.
+
+constexpr uint64_t kPairDrainLimitNs = 3 * kWaitLimitNs;
+
+template <int BN>
+struct PairTraits {
+    static constexpr int kABytes = kTcBM * kTcBK * 2;         // own 128 rows of A
+    static constexpr int kBBytes = (BN / 2) * kTcBK * 2;      // own BN/2 columns of B
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = 6;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kStoreBytes = kStoreStageBytes;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStoreBytes + kNumBars * 8 + 16;
+    static_assert(BN == 256 || BN == 128, "pair tile widths");
+    static_assert(kSmemBytes <= 227 * 1024 && kSmemBytes > 114 * 1024, "shared memory");
+    static_assert(kTmemCols <= 512, "tensor memory");
+};
+
+struct PairWaitCtx {
+    volatile uint32_t* abort_flag;   // this CTA's flag (the peer may set it remotely)
+    uint32_t peer_abort;             // shared::cluster address of the peer's flag
+};
+
+__device__ __forceinline__ void pair_raise_abort(const PairWaitCtx& w) {
+    *w.abort_flag = 1;
+    st_shared_cluster_u32(w.peer_abort, 1);
+}
+
+template <bool CLUSTER_SCOPE>
+__device__ __forceinline__ bool pair_wait_phase(uint32_t bar, uint32_t parity,
+                                                const PairWaitCtx& w, uint32_t err_bit) {
+    auto test = [&]() {
+        return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (test()) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_tc_error, err_bit);
+            pair_raise_abort(w);
+            return false;
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
+    using T = PairTraits<BN>;
+    constexpr int S = T::kStages;
+    constexpr int CW = 32;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t store_base = smem_base + S * T::kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * T::kStageBytes + T::kStoreBytes);
+    const uint32_t bar_base = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (S + s); };
+    auto accf_bar = [&](int b) { return bar_base + 8u * (2 * S + b); };
+    auto acce_bar = [&](int b) { return bar_base + 8u * (2 * S + 2 + b); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * S + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + T::kNumBars);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 8);   // four epilogue warps in each CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+        if (args.tma_store) tma_prefetch_map(&map_c);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), T::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();   // both CTAs' barriers exist and tensor memory is allocated
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const PairWaitCtx wctx{abort_flag,
+                           mapa_shared(smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u)};
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(cluster_count_x());
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer (both CTAs) ------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;
+            bool ok = true;
+            for (int u = cid; ok && u < args.num_units; u += ncl) {
+                int pb, qb, split;
+                unit_coords(args, u, pb, qb, split);
+                const int m0 = pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM;
+                const int n0 = qb * BN + static_cast<int>(rank) * (BN / 2);
+                for (int kb = 0; kb < args.kb_total; ++kb) {
+                    if (!pair_wait_phase<false>(empty_bar(stage), phase ^ 1u, wctx, kErrProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        // both CTAs' bytes complete on this barrier
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                    const uint32_t sa = smem_base + stage * T::kStageBytes;
+                    const uint32_t sb = sa + T::kABytes;
+                    const int k0 = kb * kTcBK;
+                    tma_load_2d_pair(sa, &map_a, fb, k0, m0);            // A: box {64 k, 128 rows}
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)                   // B: boxes {64 cols, 64 k}
+                        tma_load_2d_pair(sb + j * 8192, &map_b, fb, n0 + 64 * j, k0);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (leader)
+                for (int s = 0; s < S; ++s)
+                    if (armed & (1u << s)) drain_wait(full_bar(s), (armed_parity >> s) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer (even CTA) ---------------------
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = cid; ok && u < args.num_units; u += ncl) {
+                if (!pair_wait_phase<true>(acce_bar(acc), acc_phase ^ 1u, wctx, kErrMma)) break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < args.kb_total; ++kb) {
+                    if (!pair_wait_phase<false>(full_bar(stage), phase, wctx, kErrMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = smem_base + stage * T::kStageBytes;
+                    const uint32_t sb = sa + T::kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcBK / kUmmaK; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+                        tc_mma_f16_pair(d_tmem, adesc, bdesc, args.idesc,
+                                        (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(accf_bar(acc), 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            tc_commit_pair_multicast(drain_bar, 0x3);   // both CTAs learn when every MMA is done
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue (both CTAs) ----------------------
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        StoreStage stg{store_base + static_cast<uint32_t>(warp - 2) * 8192u, 0};
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = cid; u < args.num_units; u += ncl) {
+            int pb, qb, split;
+            unit_coords(args, u, pb, qb, split);
+            bool ok = pair_wait_phase<false>(accf_bar(acc), acc_phase, wctx, kErrEpilogue);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) pair_raise_abort(wctx);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t t_lane = tmem_base + static_cast<uint32_t>(acc * BN) +
+                                    (static_cast<uint32_t>(quarter * 32) << 16);
+            const int p = pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM + row;
+            const int q0 = qb * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / CW; ++c) {
+                uint32_t r[CW];
+                tmem_ld_lane_cols<CW>(t_lane + c * CW, r);
+                tmem_wait_ld();
+                if (c == BN / CW - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
+                }
+                float v[CW];
+#pragma unroll
+                for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+                if (args.tma_store)
+                    stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
+                                    pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM + quarter * 32,
+                                    args.M, args.N);
+                else
+                    store_chunk<false, CW>(args, v, p, q0 + c * CW);
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (args.tma_store && lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1 && lane == 0) {
+        // the even CTA's last commit: every pair MMA (which may read this CTA's
+        // shared memory and write its tensor memory) has finished
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain_bar, 0)) {
+            if (globaltimer_ns() - t0 > kPairDrainLimitNs) {
+                atomicOr(&g_tc_error, kErrDrain);
+                break;
+            }
+        }
+        if (*abort_flag) {
+            // give copies issued just before an abort time to land
+            const uint64_t t1 = globaltimer_ns();
+            while (globaltimer_ns() - t1 < 50000ull) {
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before_sync();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, T::kTmemCols);
+    }
+}
+
+// ---- watchdog self-test --------------------------------------------------------
+//
+// One thread waits, through the same bounded wait the GEMM kernels use, on an
+// mbarrier that nothing ever arrives on.  The wait gives up after limit_ns,
+// records kErrSelfTest in the device error word and the kernel returns: the
+// host sees GEMM_ERR_DEVICE_TIMEOUT from gemm_device_error() and the context
+// stays usable.
+
+__global__ void watchdog_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        const WaitCtx w{&abort_flag};
+        wait_phase(smem_u32(&bar), 0, w, kErrSelfTest, limit_ns);
+    }
+}
+
+cudaError_t watchdog_selftest_launch(uint64_t limit_ns, cudaStream_t stream) {
+    watchdog_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 // ---- host side --------------------------------------------------------------------
 
-bool tc_config_supported(int bn, int swap) {
+bool tc_config_supported(int bn, int swap, int pair) {
+    if (pair) return !swap && (bn == 128 || bn == 256);
     if (swap) return bn == 16 || bn == 32 || bn == 64;
     return bn == 64 || bn == 128 || bn == 256;
+}
+
+template <int BN>
+static cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairTraits<BN>::kSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int BN>
+static cudaError_t pair_max_clusters_for(int* n) {
+    auto kern = tc_gemm_pair_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairTraits<BN>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config<BN>(2, nullptr, attr);
+    return cudaOccupancyMaxActiveClusters(n, kern, &cfg);
+}
+
+cudaError_t tc_pair_max_clusters(int bn, int* n) {
+    *n = 0;
+    if (bn == 256) return pair_max_clusters_for<256>(n);
+    if (bn == 128) return pair_max_clusters_for<128>(n);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t tc_error_word(uint32_t** ptr) {
@@ -438,7 +843,7 @@ static bool encode_map(EncodeTiledFn encode, CUtensorMap* map, int fmt, const vo
 
 template <int BN, bool SWAP>
 static cudaError_t launch_cfg(const TcLaunch& L, const CUtensorMap& mp, const CUtensorMap& mq,
-                              const TcArgs& args, cudaStream_t stream) {
+                              const CUtensorMap& mc, const TcArgs& args, cudaStream_t stream) {
     using T = TcTraits<BN, SWAP>;
     auto kern = tc_gemm_kernel<BN, SWAP>;
     // The attribute is per device; setting it every call is cheap and keeps
@@ -446,12 +851,25 @@ static cudaError_t launch_cfg(const TcLaunch& L, const CUtensorMap& mp, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, kThreads, T::kSmemBytes, stream>>>(mp, mq, args);
+    kern<<<L.grid, kThreads, T::kSmemBytes, stream>>>(mp, mq, mc, args);
     return cudaGetLastError();
 }
 
+template <int BN>
+static cudaError_t launch_pair(const TcLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb,
+                               const CUtensorMap& mc, const TcArgs& args, cudaStream_t stream) {
+    auto kern = tc_gemm_pair_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairTraits<BN>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config<BN>(L.grid, stream, attr);
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, args);
+}
+
 cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t stream) {
-    if (!tc_config_supported(L.bn, L.swap)) return cudaErrorInvalidValue;
+    if (!tc_config_supported(L.bn, L.swap, L.pair)) return cudaErrorInvalidValue;
+    if (L.pair && (L.splits != 1 || (L.grid & 1))) return cudaErrorInvalidValue;
     // A: {K, M} (K contiguous); B: {N, K} (N contiguous).
     CUtensorMap map_a, map_b;
     const uint32_t a_rows = L.swap ? static_cast<uint32_t>(L.bn) : kTcBM;
@@ -467,7 +885,7 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.N = static_cast<int32_t>(L.N);
     const int64_t pe = L.swap ? L.N : L.M;
     const int64_t qe = L.swap ? L.M : L.N;
-    a.tiles_p = static_cast<int32_t>(ceil_div(pe, kTcBM));
+    a.tiles_p = static_cast<int32_t>(ceil_div(pe, L.pair ? 2 * kTcBM : kTcBM));
     a.tiles_q = static_cast<int32_t>(ceil_div(qe, L.bn));
     a.kb_total = static_cast<int32_t>(ceil_div(L.K, kTcBK));
     a.splits = L.splits;
@@ -475,24 +893,50 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.num_units = a.tiles_p * a.tiles_q * L.splits;
     a.group = L.group;
     a.vec_store = ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0 && (L.ldc & 3) == 0) ? 1 : 0;
-    a.idesc = idesc_f16_f32(static_cast<uint32_t>(L.fmt), L.swap != 0, L.swap == 0, kTcBM,
-                            static_cast<uint32_t>(L.bn));
+    // C through TMA stores: FP32 {N, M}, row stride ldc * 4 bytes, box 32 x 32,
+    // 128-byte swizzle (needs a 16-byte aligned base and row stride).  The
+    // store clips a box at C's last column only to a 16-byte boundary, so it
+    // is used only when rows end on one (N a multiple of 4): otherwise the
+    // columns between N and the boundary -- the caller's padding -- would be
+    // written.
+    CUtensorMap map_c;
+    memset(&map_c, 0, sizeof(map_c));
+    a.tma_store = 0;
+    if (!L.swap && a.vec_store && (L.N % 4) == 0) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.N), static_cast<cuuint64_t>(L.M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.ldc) * 4};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&map_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, L.C, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            a.tma_store = (L.store_mode == 1) ? 0 : 1;
+    }
+    a.idesc = idesc_f16_f32(static_cast<uint32_t>(L.fmt), L.swap != 0, L.swap == 0,
+                            L.pair ? 2 * kTcBM : kTcBM, static_cast<uint32_t>(L.bn));
     a.ws = L.ws;
     a.counters = L.counters;
 
     const CUtensorMap& mp = L.swap ? map_b : map_a;
     const CUtensorMap& mq = L.swap ? map_a : map_b;
+    if (L.pair) {
+        switch (L.bn) {
+            case 128: return launch_pair<128>(L, map_a, map_b, map_c, a, stream);
+            case 256: return launch_pair<256>(L, map_a, map_b, map_c, a, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (!L.swap) {
         switch (L.bn) {
-            case 64: return launch_cfg<64, false>(L, mp, mq, a, stream);
-            case 128: return launch_cfg<128, false>(L, mp, mq, a, stream);
-            case 256: return launch_cfg<256, false>(L, mp, mq, a, stream);
+            case 64: return launch_cfg<64, false>(L, mp, mq, map_c, a, stream);
+            case 128: return launch_cfg<128, false>(L, mp, mq, map_c, a, stream);
+            case 256: return launch_cfg<256, false>(L, mp, mq, map_c, a, stream);
         }
     } else {
         switch (L.bn) {
-            case 16: return launch_cfg<16, true>(L, mp, mq, a, stream);
-            case 32: return launch_cfg<32, true>(L, mp, mq, a, stream);
-            case 64: return launch_cfg<64, true>(L, mp, mq, a, stream);
+            case 16: return launch_cfg<16, true>(L, mp, mq, map_c, a, stream);
+            case 32: return launch_cfg<32, true>(L, mp, mq, map_c, a, stream);
+            case 64: return launch_cfg<64, true>(L, mp, mq, map_c, a, stream);
         }
     }
     return cudaErrorInvalidValue;

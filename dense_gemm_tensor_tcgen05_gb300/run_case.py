@@ -26,6 +26,7 @@ def main():
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--swap-ab", type=int, default=-1)
     ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--cta-pair", type=int, default=0)
     a = ap.parse_args()
 
     import numpy as np
@@ -47,7 +48,8 @@ def main():
     Cd = torch.empty((a.M, a.N), dtype=torch.float32, device="cuda")
     code = {"f16": 0, "bf16": 1, "f32": 2}[a.dtype]
     opts = {k: v for k, v in dict(tile_n=a.tile_n, split_k=a.split_k, swap_ab=a.swap_ab,
-                                  group_m=a.group_m).items() if v not in (0, -1)}
+                                  group_m=a.group_m, cta_pair=a.cta_pair).items()
+            if v not in (0, -1)}
     args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), a.M, a.N, a.K, a.K, a.N, a.N)
     s = torch.cuda.current_stream().cuda_stream
     if opts:

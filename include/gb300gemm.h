@@ -113,7 +113,12 @@ gemm_status_t sgemm_f32(const float *A, const float *B, float *C,
  *   swap_ab   -1 = planner, 0 = never, 1 = compute C^T = B^T A^T so that N
  *             runs along the 128-row MMA side (for small M).
  *   generic   1 = force the CUDA-core kernel (any alignment).
- *   group_m   tiles per raster group along the 128-row side (0 = planner).
+ *   group_m   tiles per raster group along the MMA's M side (0 = planner).
+ *   cta_pair  0 = planner, 1 = one CTA per 128-row tile, 2 = CTA pairs
+ *             (clusters of two SMs sharing a 256-row tile; tile_n 128 or
+ *             256, no swap, no split-K).
+ *   store_mode 0 = planner (tensor-core results leave through TMA stores
+ *             when C's base, ldc and N allow it), 1 = plain stores.
  * Invalid combinations return GEMM_ERR_INVALID_VALUE.
  */
 typedef struct {
@@ -123,7 +128,8 @@ typedef struct {
     int32_t swap_ab;
     int32_t generic;
     int32_t group_m;
-    int32_t reserved[2];
+    int32_t cta_pair;
+    int32_t store_mode;
 } gemm_options_t;
 
 /* gemm_ex -- the same operation with an explicit plan (tests and tuning). */
@@ -153,9 +159,44 @@ gemm_status_t gemm_plan_describe(int32_t dtype, const void *A, const void *B, co
  */
 gemm_status_t gemm_device_error(gemm_stream_t stream);
 
+/*
+ * gemm_watchdog_selftest -- checks the failure path of the kernels' pipeline
+ * waits.  Enqueues on `stream` one small kernel whose single wait can never
+ * be satisfied; the wait gives up after limit_ms (1..2000) milliseconds,
+ * through the same bounded wait the GEMM kernels use, and records the fact
+ * in the device error word.  A following gemm_device_error(stream) returns
+ * GEMM_ERR_DEVICE_TIMEOUT (and clears the word); the context stays usable.
+ * No GEMM is affected.  (A testing aid of this library; the pages have no
+ * counterpart.)
+ */
+gemm_status_t gemm_watchdog_selftest(int32_t limit_ms, gemm_stream_t stream);
+
 /* gemm_release_workspace -- frees the split-K workspaces of the current
  * device after synchronising the device.  Later calls allocate again. */
 gemm_status_t gemm_release_workspace(void);
+
+/*
+ * gemm_ex_host -- the same operation with A, B and C in HOST memory.
+ *
+ * The library copies B to the device once, then cuts M into row panels and,
+ * for each panel, copies the A rows in, runs the product (the kernels of
+ * gemm_ex, on `stream`) and copies the C rows back, with the copies of one
+ * panel overlapping the product of the next (two internal copy streams).
+ * For the copies to overlap, A, B and C must be page-locked (cudaHostAlloc /
+ * cudaHostRegister); pageable memory works but serialises.  Leading
+ * dimensions are those of the host arrays.
+ *
+ * The call returns after enqueueing; C is complete when `stream` reaches
+ * this point (synchronise `stream` before reading C).  Work already queued on
+ * `stream` finishes before the copies start.  Device staging buffers (B, two
+ * A panels, two C panels), the copy streams and events belong to the library,
+ * one set per (device, stream), allocated on first use and grown as needed;
+ * gemm_release_workspace() does not free them.
+ */
+gemm_status_t gemm_ex_host(const void *A, const void *B, float *C,
+                           int64_t M, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldc,
+                           const gemm_options_t *options, gemm_stream_t stream);
 
 /*
  * gemm_ex_noalloc -- gemm_ex for callers that cannot allocate device memory.

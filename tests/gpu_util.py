@@ -45,7 +45,9 @@ def run_gpu(dt, A_bits, B_bits, M, N, K, lda=None, ldb=None, ldc=None, offsets=(
     Ad = to_device(A_bits, dt, offsets[0])
     Bd = to_device(B_bits, dt, offsets[1])
     rows = max(M, 1)
-    cbuf = torch.full((rows * ldc + offsets[2] + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    guard = 4096   # NaN floats after C: a write past C's last row shows up here
+    cbuf = torch.full((rows * ldc + offsets[2] + guard,), float("nan"), dtype=torch.float32,
+                      device="cuda")
     Cd = cbuf[offsets[2]:]
     st = stream if stream is not None else torch.cuda.current_stream()
     sh = st.cuda_stream
@@ -56,6 +58,10 @@ def run_gpu(dt, A_bits, B_bits, M, N, K, lda=None, ldb=None, ldc=None, offsets=(
     else:
         {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32}[dt](*args, stream=sh)
     g.gemm_device_error(sh)
+    tail = Cd[rows * ldc:].cpu().numpy()
+    assert np.all(np.isnan(tail)), "kernel wrote past the end of C"
+    if offsets[2]:
+        assert torch.isnan(cbuf[:offsets[2]]).all().item(), "kernel wrote before the start of C"
     C = Cd[: rows * ldc].reshape(rows, ldc).cpu().numpy()[:M]
     if ldc > N and M > 0:
         assert np.all(np.isnan(C[:, N:])), "kernel wrote into C's padding columns"

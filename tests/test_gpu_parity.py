@@ -47,6 +47,8 @@ TC_CONFIGS = [
     dict(tile_n=64, swap_ab=0, split_k=7), dict(tile_n=16, swap_ab=1, split_k=4),
     dict(tile_n=64, swap_ab=1, split_k=5), dict(tile_n=128, swap_ab=0, split_k=1, group_m=1),
     dict(tile_n=256, swap_ab=0, split_k=1, group_m=3),
+    dict(cta_pair=2, tile_n=256), dict(cta_pair=2, tile_n=128),
+    dict(cta_pair=2, tile_n=256, group_m=1), dict(cta_pair=1, tile_n=256),
 ]
 
 
@@ -266,6 +268,92 @@ def test_matmul_with_host_buffers():
     assert cmp.ok, str(cmp)
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(256, 256, 64), (257, 255, 65), (1024, 1280, 2048),
+                                   (130, 700, 300), (600, 260, 4100)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cta_pair_kernel(dt, shape):
+    M, N, K = shape
+    gu.check_full(dt, "small_int", M, N, K, exact=True, cta_pair=2)
+    gu.check_full(dt, "normal", M, N, K, seed=3, cta_pair=2)
+
+
+MULTI_TILE_PLANS = [dict(cta_pair=1, tile_n=256), dict(cta_pair=1, tile_n=128),
+                    dict(cta_pair=1, tile_n=64), dict(cta_pair=2, tile_n=256),
+                    dict(cta_pair=2, tile_n=128), dict(cta_pair=1, tile_n=256, store_mode=1),
+                    dict(cta_pair=2, tile_n=256, store_mode=1)]
+
+
+@pytest.mark.parametrize("cfg", MULTI_TILE_PLANS, ids=_cfg_id)
+@pytest.mark.parametrize("shape", [(4000, 3000, 1000), (4000, 2248, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_multi_tile_ragged_every_plan(cfg, shape):
+    # several tiles per CTA with ragged M and N; (4000, 2248, 512) leaves a
+    # single 32-column chunk of the last 256-wide tile wholly past N
+    M, N, K = shape
+    gu.check_full("f16", "small_int", M, N, K, exact=True, **cfg)
+    gu.check_full("bf16", "uniform", M, N, K, seed=4, **cfg)
+
+
+def test_cta_pair_many_units_per_cluster():
+    # more pair tiles than resident clusters: every cluster loops over several
+    # tiles and both accumulators
+    gu.check_full("bf16", "small_int", 4096, 4096, 256, exact=True, cta_pair=2)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_gemm_ex_host_pipeline(dt, pinned):
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    M, N, K = 2600, 384, 520          # four row panels, the last one ragged
+    lda, ldb, ldc = K + 8, N + 4, N + 4
+    A, B = gu.make_inputs(dt, "small_int", M, N, K, 0)
+    Ap, Bp = inputs.padded(A, lda), inputs.padded(B, ldb)
+    Ch = np.full((M, ldc), np.nan, dtype=np.float32)
+    if pinned:
+        At = torch.from_numpy(Ap.view(np.int32 if dt == "f32" else np.int16)).pin_memory()
+        Bt = torch.from_numpy(Bp.view(np.int32 if dt == "f32" else np.int16)).pin_memory()
+        Ct = torch.from_numpy(Ch).pin_memory()
+        ptrs = (At.data_ptr(), Bt.data_ptr(), Ct.data_ptr())
+    else:
+        Ct = None
+        ptrs = (Ap.ctypes.data, Bp.ctypes.data, Ch.ctypes.data)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):   # the second call reuses the library's staging buffers
+        g.gemm_ex_host(*ptrs, M, N, K, lda, ldb, ldc, dtype=gu.CODE[dt], stream=stream.cuda_stream)
+        stream.synchronize()
+        C = Ct.numpy() if pinned else Ch
+        R = oracle.gemm(dt, A, B)
+        assert np.array_equal(C[:, :N], R.astype(np.float32))
+        assert np.all(np.isnan(C[:, N:]))
+
+
+def test_matmul_host_uses_pipeline():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    A, B = gu.make_inputs("f16", "uniform", 1500, 256, 300, 8)
+    At = torch.from_numpy(A.view(np.int16)).view(torch.float16)
+    Bt = torch.from_numpy(B.view(np.int16)).view(torch.float16)
+    C = g.matmul(At, Bt)
+    R = oracle.gemm("f16", A, B)
+    cmp = oracle.compare(C.numpy(), R, 300, inputs.bits_abs_max(A, "f16"), inputs.bits_abs_max(B, "f16"))
+    assert cmp.ok, str(cmp)
+
+
+def test_watchdog_gives_up_and_context_stays_usable():
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    s = torch.cuda.current_stream().cuda_stream
+    g.gemm_device_error(s)                          # start from a clear error word
+    g.gemm_watchdog_selftest(20, s)                 # a wait nothing satisfies, 20 ms limit
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_device_error(s)
+    assert e.value.name == "GEMM_ERR_DEVICE_TIMEOUT"
+    g.gemm_device_error(s)                          # the word was cleared
+    gu.check_full("bf16", "small_int", 300, 520, 700, exact=True)   # GEMMs still work
+
+
 def test_plan_describe_routes():
     import torch
     import dense_gemm_tensor_tcgen05_gb300 as g
@@ -275,6 +363,7 @@ def test_plan_describe_routes():
         B = torch.empty((K, N), dtype=gu.torch_dtype(dt), device="cuda")
         return g.plan(A, B)
     assert plan("bf16", 8192, 8192, 8192).startswith("tcgen05")
+    assert "pair=1" in plan("bf16", 8192, 8192, 8192)
     assert "swap=1" in plan("f16", 8, 8192, 8192)
     assert plan("f32", 4096, 4096, 4096).startswith("sgemm")
     assert plan("f16", 10, 10, 7).startswith("generic")   # lda = 7: no TMA
