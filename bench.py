@@ -47,7 +47,7 @@ METRIC = "GEMM TFLOP/s (FP16-in/FP32-acc, M=N=K=8192) and % of GB300 dense peak"
 SEED = 1238
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_bf16_8192_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_gemm_tensor_tcgen05_gb300", "csrc", f)
-                  for f in ("tc_gemm.cu", "ptx.cuh", "api.cu", "internal.h")]
+                  for f in ("tc_gemm.cu", "ptx.cuh")]
 
 
 def kernel_source_hash() -> str:
@@ -71,17 +71,23 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def load_traffic():
+def load_traffic(plan: str):
     """DRAM bytes per launch from the committed ncu capture, if it was taken
-    on the current kernel sources; else None."""
+    on the current kernel sources with the same plan; else None."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("source_hash") != kernel_source_hash():
+    if t.get("source_hash") != kernel_source_hash() or t.get("plan") != plan:
         return None
     return t.get("dram_bytes_per_launch")
+
+
+def kernel_name(plan: str) -> str:
+    if "pair=1" in plan:
+        return "tc_gemm_pair_kernel<256> (CTA pairs, 256x256 tiles)"
+    return "tc_gemm_kernel<256,false> (one CTA, 128x256 tiles)"
 
 
 # ---- clocks ---------------------------------------------------------------
@@ -286,9 +292,9 @@ def run_gb300(args, rank, world, local_rank):
     achieved = FLOP / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": load_traffic(),
+                "traffic": load_traffic(plan),
                 "peak_source": f"bf16_tflops (burst) of {peaks['source']}",
-                "kernel": "tc_gemm_kernel<256,false>", "kernel_ms_mean": kernel_ms,
+                "kernel": kernel_name(plan), "kernel_ms_mean": kernel_ms,
                 "kernel_ms_median": statistics.median(per),
                 "kernel_ms_first_tenth": statistics.mean(per[: max(1, len(per) // 10)]),
                 "kernel_ms_last_tenth": statistics.mean(per[-max(1, len(per) // 10):]),

@@ -774,20 +774,22 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
 
 // ---- host-buffer entry point -------------------------------------------------------
 //
-// gemm_ex_host: A, B and C in host memory.  B is copied to the device once;
-// then M is cut into row panels and, per panel, the A rows go in, the product
-// runs, and the C rows come back -- on three streams (copy in, compute = the
-// caller's stream, copy out) with two device buffers per panel operand, so
-// the copies of one panel overlap the product of the next.  Device staging
-// buffers, the two copy streams and the events are owned by the library, one
-// set per (device, caller stream), allocated on first use and grown as needed.
+// gemm_ex_host: A, B and C in host memory.  C is cut into blocks of row
+// panels (of A) by column panels (of B).  The copies in (A panels; B panels
+// while the first row panel is being computed), the products (the caller's
+// stream) and the copies out (C blocks) run on three streams, so the first C
+// block starts back after only a quarter of A and of B have arrived and the
+// two copy directions overlap each other and the products.  Device staging
+// buffers (B whole, two A row panels, two C row panels), the two copy
+// streams and the events belong to the library, one set per (device, caller
+// stream), allocated on first use and grown as needed.
 
 namespace {
 
 struct HostPipe {
     cudaStream_t s_in = nullptr, s_out = nullptr;
-    cudaEvent_t e_start = nullptr;
-    cudaEvent_t e_in[2] = {}, e_comp[2] = {}, e_out[2] = {};
+    cudaEvent_t e_start = nullptr, e_a = nullptr, e_b = nullptr, e_blk = nullptr;
+    cudaEvent_t e_rowcomp[2] = {}, e_rowout[2] = {};
     void* dB = nullptr;
     size_t dB_bytes = 0;
     void* dA[2] = {};
@@ -821,16 +823,15 @@ gemm_status_t host_pipe(int dev, cudaStream_t stream, size_t b_bytes, size_t a_b
     HostPipe& h = g_hp[{dev, stream}];
     cudaError_t e = cudaSuccess;
     if (!h.s_in) {
+        cudaEvent_t* evs[] = {&h.e_start, &h.e_a, &h.e_b, &h.e_blk, &h.e_rowcomp[0],
+                              &h.e_rowcomp[1], &h.e_rowout[0], &h.e_rowout[1]};
         if ((e = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&h.e_start, cudaEventDisableTiming)) != cudaSuccess) {
+            (e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking)) != cudaSuccess) {
             note_cuda_error(e, "host pipeline streams");
             return GEMM_ERR_CUDA;
         }
-        for (int i = 0; i < 2; ++i) {
-            if ((e = cudaEventCreateWithFlags(&h.e_in[i], cudaEventDisableTiming)) != cudaSuccess ||
-                (e = cudaEventCreateWithFlags(&h.e_comp[i], cudaEventDisableTiming)) != cudaSuccess ||
-                (e = cudaEventCreateWithFlags(&h.e_out[i], cudaEventDisableTiming)) != cudaSuccess) {
+        for (cudaEvent_t* ev : evs) {
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) {
                 note_cuda_error(e, "host pipeline events");
                 return GEMM_ERR_CUDA;
             }
@@ -857,12 +858,12 @@ gemm_status_t host_pipe(int dev, cudaStream_t stream, size_t b_bytes, size_t a_b
     return GEMM_OK;
 }
 
-// Rows per panel: enough that each panel's product still fills the GPU with
-// several waves of tiles, at most four panels' worth of overlap to win.
-int64_t panel_rows(int64_t M) {
-    if (M <= 1024) return M;
-    int64_t rows = ceil_div(ceil_div(M, 4), 256) * 256;
-    return rows < 512 ? 512 : rows;
+// Panel extent along one dimension: a quarter, rounded up to 256, at least
+// 512; extents up to 1024 stay whole.
+int64_t panel_extent(int64_t n) {
+    if (n <= 1024) return n;
+    int64_t e = ceil_div(ceil_div(n, 4), 256) * 256;
+    return e < 512 ? 512 : e;
 }
 
 }  // namespace
@@ -883,9 +884,9 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
     if (st != GEMM_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
 
-    const int64_t prow = panel_rows(M);
-    const int64_t npanels = ceil_div(M, prow);
-    // device layouts are dense: ld = K for A panels, N for B and C panels
+    const int64_t prow = panel_extent(M), pcol = panel_extent(N);
+    const int64_t nrow = ceil_div(M, prow), ncol = ceil_div(N, pcol);
+    // device layouts are dense: ld = K for A panels, N for B and the C panels
     const size_t b_bytes = static_cast<size_t>(std::max<int64_t>(K, 1) * N) * es;
     const size_t a_bytes = static_cast<size_t>(prow * std::max<int64_t>(K, 1)) * es;
     const size_t c_bytes = static_cast<size_t>(prow * N) * 4;
@@ -909,36 +910,47 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
     HP_CHECK(cudaEventRecord(h->e_start, stream), "cudaEventRecord");
     HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_start, 0), "cudaStreamWaitEvent");
     HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_start, 0), "cudaStreamWaitEvent");
-    if (K > 0)
-        HP_CHECK(cudaMemcpy2DAsync(h->dB, N * es, B, ldb * es, N * es, K, cudaMemcpyHostToDevice,
-                                   h->s_in),
-                 "cudaMemcpy2DAsync(B)");
-    for (int64_t i = 0; i < npanels; ++i) {
+    for (int64_t i = 0; i < nrow; ++i) {
         const int buf = static_cast<int>(i & 1);
         const int64_t r0 = i * prow;
         const int64_t rows = std::min<int64_t>(prow, M - r0);
-        if (i >= 2) HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_comp[buf], 0), "cudaStreamWaitEvent");
+        // A panel i into buffer `buf`, once row panel i - 2 is no longer read
+        if (i >= 2) HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_rowcomp[buf], 0), "cudaStreamWaitEvent");
         if (K > 0)
             HP_CHECK(cudaMemcpy2DAsync(h->dA[buf], K * es, static_cast<const char*>(A) + r0 * lda * es,
                                        lda * es, K * es, rows, cudaMemcpyHostToDevice, h->s_in),
                      "cudaMemcpy2DAsync(A panel)");
-        HP_CHECK(cudaEventRecord(h->e_in[buf], h->s_in), "cudaEventRecord");
-        HP_CHECK(cudaStreamWaitEvent(stream, h->e_in[buf], 0), "cudaStreamWaitEvent");
-        if (i >= 2) HP_CHECK(cudaStreamWaitEvent(stream, h->e_out[buf], 0), "cudaStreamWaitEvent");
-        st = run(dtype, h->dA[buf], h->dB, static_cast<float*>(h->dC[buf]), rows, N, K, K, N, N,
-                 *options, stream);
-        if (st != GEMM_OK) return st;
-        HP_CHECK(cudaEventRecord(h->e_comp[buf], stream), "cudaEventRecord");
-        HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_comp[buf], 0), "cudaStreamWaitEvent");
-        HP_CHECK(cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, h->dC[buf], N * 4, N * 4, rows,
-                                   cudaMemcpyDeviceToHost, h->s_out),
-                 "cudaMemcpy2DAsync(C panel)");
-        HP_CHECK(cudaEventRecord(h->e_out[buf], h->s_out), "cudaEventRecord");
+        HP_CHECK(cudaEventRecord(h->e_a, h->s_in), "cudaEventRecord");
+        HP_CHECK(cudaStreamWaitEvent(stream, h->e_a, 0), "cudaStreamWaitEvent");
+        // C panel buffer `buf` is free once row panel i - 2 has been copied out
+        if (i >= 2) HP_CHECK(cudaStreamWaitEvent(stream, h->e_rowout[buf], 0), "cudaStreamWaitEvent");
+        for (int64_t j = 0; j < ncol; ++j) {
+            const int64_t c0 = j * pcol;
+            const int64_t cols = std::min<int64_t>(pcol, N - c0);
+            if (i == 0 && K > 0) {
+                // B column panel j, the first time it is needed
+                HP_CHECK(cudaMemcpy2DAsync(static_cast<char*>(h->dB) + c0 * es, N * es,
+                                           static_cast<const char*>(B) + c0 * es, ldb * es,
+                                           cols * es, K, cudaMemcpyHostToDevice, h->s_in),
+                         "cudaMemcpy2DAsync(B panel)");
+                HP_CHECK(cudaEventRecord(h->e_b, h->s_in), "cudaEventRecord");
+                HP_CHECK(cudaStreamWaitEvent(stream, h->e_b, 0), "cudaStreamWaitEvent");
+            }
+            float* cblk = static_cast<float*>(h->dC[buf]) + c0;
+            st = run(dtype, h->dA[buf], static_cast<const char*>(h->dB) + c0 * es, cblk, rows, cols,
+                     K, K, N, N, *options, stream);
+            if (st != GEMM_OK) return st;
+            HP_CHECK(cudaEventRecord(h->e_blk, stream), "cudaEventRecord");
+            HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_blk, 0), "cudaStreamWaitEvent");
+            HP_CHECK(cudaMemcpy2DAsync(C + r0 * ldc + c0, ldc * 4, cblk, N * 4, cols * 4, rows,
+                                       cudaMemcpyDeviceToHost, h->s_out),
+                     "cudaMemcpy2DAsync(C block)");
+        }
+        HP_CHECK(cudaEventRecord(h->e_rowcomp[buf], stream), "cudaEventRecord");
+        HP_CHECK(cudaEventRecord(h->e_rowout[buf], h->s_out), "cudaEventRecord");
     }
-    // later work on `stream` (and the caller's synchronisation) sees C
-    const int last = static_cast<int>((npanels - 1) & 1);
-    HP_CHECK(cudaStreamWaitEvent(stream, h->e_out[last], 0), "cudaStreamWaitEvent");
-    if (npanels >= 2) HP_CHECK(cudaStreamWaitEvent(stream, h->e_out[last ^ 1], 0), "cudaStreamWaitEvent");
+    // later work on `stream` (and the caller's synchronisation) sees all of C
+    HP_CHECK(cudaStreamWaitEvent(stream, h->e_rowout[(nrow - 1) & 1], 0), "cudaStreamWaitEvent");
 #undef HP_CHECK
     return GEMM_OK;
 }

@@ -178,10 +178,12 @@ gemm_status_t gemm_release_workspace(void);
 /*
  * gemm_ex_host -- the same operation with A, B and C in HOST memory.
  *
- * The library copies B to the device once, then cuts M into row panels and,
- * for each panel, copies the A rows in, runs the product (the kernels of
- * gemm_ex, on `stream`) and copies the C rows back, with the copies of one
- * panel overlapping the product of the next (two internal copy streams).
+ * The library cuts C into blocks of A row panels by B column panels (up to
+ * four of each).  It copies an A panel in, the B panels the first time they
+ * are needed, runs each block's product (the kernels of gemm_ex, on
+ * `stream`) and copies each C block back as soon as it is done, on two
+ * internal copy streams, so the two copy directions overlap each other and
+ * the products.
  * For the copies to overlap, A, B and C must be page-locked (cudaHostAlloc /
  * cudaHostRegister); pageable memory works but serialises.  Leading
  * dimensions are those of the host arrays.

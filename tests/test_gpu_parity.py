@@ -303,10 +303,12 @@ def test_cta_pair_many_units_per_cluster():
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
-def test_gemm_ex_host_pipeline(dt, pinned):
+@pytest.mark.parametrize("shape", [(2600, 384, 520), (2600, 2100, 300), (700, 3000, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_ex_host_pipeline(dt, pinned, shape):
     import torch
     import dense_gemm_tensor_tcgen05_gb300 as g
-    M, N, K = 2600, 384, 520          # four row panels, the last one ragged
+    M, N, K = shape    # row panels and column panels, the last ones ragged
     lda, ldb, ldc = K + 8, N + 4, N + 4
     A, B = gu.make_inputs(dt, "small_int", M, N, K, 0)
     Ap, Bp = inputs.padded(A, lda), inputs.padded(B, ldb)
