@@ -64,7 +64,8 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
                 ("generic", ctypes.c_int32), ("group_m", ctypes.c_int32),
-                ("cta_pair", ctypes.c_int32), ("store_mode", ctypes.c_int32)]
+                ("cta_pair", ctypes.c_int32), ("store_mode", ctypes.c_int32),
+                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 _lock = threading.Lock()
@@ -141,11 +142,11 @@ def sgemm_f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int
 
 
 def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0,
-             cta_pair=0, store_mode=0) -> GemmOptions:
+             cta_pair=0, store_mode=0, stream_k=0) -> GemmOptions:
     o = GemmOptions()
     o.dtype, o.tile_n, o.split_k, o.swap_ab, o.generic, o.group_m = (
         dtype, tile_n, split_k, swap_ab, generic, group_m)
-    o.cta_pair, o.store_mode = cta_pair, store_mode
+    o.cta_pair, o.store_mode, o.stream_k = cta_pair, store_mode, stream_k
     return o
 
 

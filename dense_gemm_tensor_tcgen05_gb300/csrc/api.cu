@@ -371,6 +371,29 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     const int64_t tiles = tiles_p * ceil_div(qe, L.bn);
     const int64_t kb_total = ceil_div(K, kTcBK);
 
+    if (o.stream_k < 0 || o.stream_k > 2) return GEMM_ERR_INVALID_VALUE;
+    int64_t group = o.group_m > 0 ? o.group_m : 16;
+    if (group > tiles_p) group = tiles_p;
+    L.group = static_cast<int>(group);
+
+    if (o.split_k <= 0 && o.stream_k == 2) {
+        // Stream-K: whole tiles while whole waves last, then the remaining
+        // tiles' k-blocks shared evenly by every CTA (partial tiles summed in
+        // a fixed order), so no SM idles through a partial last wave.  Opt-in:
+        // on the measured shapes the sum of a split tile's pieces, one L2 round
+        // trip per 32-column chunk and piece, costs more than the idle SMs
+        // of the last wave.
+        const int64_t slot_tiles = tc_streamk_schedule(L, tiles, kb_total, sms);
+        p.units = tiles;
+        if (slot_tiles > 0) {
+            p.ws_floats = static_cast<size_t>(slot_tiles * L.max_seg * kTcBM * L.bn);
+            p.n_counters = static_cast<size_t>(slot_tiles * 4);
+        }
+        p.kind = Kind::Tc;
+        *plan = p;
+        return GEMM_OK;
+    }
+
     int64_t splits = 1;
     if (o.split_k > 0) {
         if (o.split_k > 64) return GEMM_ERR_INVALID_VALUE;
@@ -392,10 +415,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     const int64_t kb_per = ceil_div(kb_total, splits);
     splits = ceil_div(kb_total, kb_per);   // no empty slices
     L.splits = static_cast<int>(splits);
-
-    int64_t group = o.group_m > 0 ? o.group_m : 16;
-    if (group > tiles_p) group = tiles_p;
-    L.group = static_cast<int>(group);
+    L.max_seg = L.splits;
 
     p.units = tiles * splits;
     L.grid = static_cast<int>(std::min<int64_t>(p.units, sms));
@@ -427,10 +447,18 @@ void describe(const Plan& p, int dtype, char* buf, int64_t size) {
             break;
         }
         case Kind::Tc:
-            snprintf(buf, n,
-                     "tcgen05 fmt=%s tile=%dx%d pair=%d swap=%d split_k=%d group=%d units=%lld grid=%d",
-                     p.tc.fmt ? "bf16" : "f16", p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
-                     p.tc.swap, p.tc.splits, p.tc.group, static_cast<long long>(p.units), p.tc.grid);
+            if (p.tc.sk_mode)
+                snprintf(buf, n,
+                         "tcgen05 fmt=%s tile=%dx%d pair=%d swap=%d stream_k dp_tiles=%d sk_kblocks=%lld "
+                         "max_seg=%d group=%d units=%lld grid=%d",
+                         p.tc.fmt ? "bf16" : "f16", p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
+                         p.tc.swap, p.tc.dp_tiles, static_cast<long long>(p.tc.sk_kblocks),
+                         p.tc.max_seg, p.tc.group, static_cast<long long>(p.units), p.tc.grid);
+            else
+                snprintf(buf, n,
+                         "tcgen05 fmt=%s tile=%dx%d pair=%d swap=%d split_k=%d group=%d units=%lld grid=%d",
+                         p.tc.fmt ? "bf16" : "f16", p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
+                         p.tc.swap, p.tc.splits, p.tc.group, static_cast<long long>(p.units), p.tc.grid);
             break;
     }
 }
@@ -479,7 +507,7 @@ gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, 
                          "cuTensorMapEncodeTiled entry point unavailable");
                 return GEMM_ERR_CUDA;
             }
-            if (p.tc.splits > 1) {
+            if (p.ws_floats) {
                 st = get_workspace(dev, stream, p.ws_floats, p.n_counters, &p.tc.ws, &p.tc.counters);
                 if (st != GEMM_OK) return st;
             }
@@ -762,7 +790,7 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
                          "cuTensorMapEncodeTiled entry point unavailable");
                 return GEMM_ERR_CUDA;
             }
-            if (p.tc.splits > 1) {
+            if (p.ws_floats) {
                 st = noalloc_bind_scratch(dev, p, stream, &p.tc.ws, &p.tc.counters);
                 if (st != GEMM_OK) return st;
             }

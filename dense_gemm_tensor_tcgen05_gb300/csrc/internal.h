@@ -24,7 +24,11 @@ struct TcLaunch {
     int swap;       // 1: MMA M side runs along N of C (C^T = B^T A^T)
     int pair;       // 1: CTA-pair kernel (clusters of 2, 256 x bn tiles)
     int store_mode;    // 0: TMA stores when C allows them, 1: plain stores
-    int splits;     // K slices
+    int splits;     // K slices (split schedule)
+    int sk_mode;    // 1: stream-K schedule (data-parallel tiles, then shared k-blocks)
+    int dp_tiles;   // stream-K: tiles done whole
+    int64_t sk_kblocks;  // stream-K: k-blocks shared out over the grid
+    int max_seg;    // workspace slots per split tile
     int group;      // raster group height in tiles along the MMA M side
     int grid;       // CTAs (persistent); <= units
     float* ws;          // split-K partial tiles (splits * tiles * 128 * bn floats), or null
@@ -36,6 +40,11 @@ constexpr int kTcBM = 128;  // rows along the MMA M side (= tensor-memory lanes)
 constexpr int kTcBK = 64;   // k per pipeline stage (64 16-bit elements = 128 bytes)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Stream-K schedule of the one-CTA kernel for `tiles` tiles of `kb_total`
+// k-blocks on at most `sms` CTAs: fills dp_tiles, sk_kblocks, max_seg, grid
+// of L and returns the number of tiles that need workspace slots.
+int64_t tc_streamk_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sms);
 
 // Which (bn, swap, pair) kernels exist.
 bool tc_config_supported(int bn, int swap, int pair);
@@ -62,7 +71,11 @@ cudaError_t tc_error_word(uint32_t** ptr);
 struct SgemmPart {
     int tile0;      // first linear tile
     int tiles;      // tiles in this launch
-    int splits;     // K slices per tile
+    int splits;     // K slices (split schedule)
+    int sk_mode;    // 1: stream-K schedule (data-parallel tiles, then shared k-blocks)
+    int dp_tiles;   // stream-K: tiles done whole
+    int64_t sk_kblocks;  // stream-K: k-blocks shared out over the grid
+    int max_seg;    // workspace slots per split tile per tile
     int k_chunk;    // K per slice (multiple of the kernel's K step)
 };
 

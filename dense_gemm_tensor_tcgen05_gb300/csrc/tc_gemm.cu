@@ -42,6 +42,7 @@
 // the producer waits (bounded) for its own TMA copies and the MMA thread for
 // its own MMAs, and tensor memory is freed on every path.
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 
@@ -65,8 +66,12 @@ struct TcArgs {
     int64_t ldc;
     int32_t M, N;
     int32_t tiles_p, tiles_q;   // tiles along the MMA M side / N side
-    int32_t num_units;          // tiles * splits
+    int32_t num_units;          // tiles * splits (split schedule)
     int32_t splits, kb_total, kb_per_split;
+    int32_t sk_mode;            // 1: data-parallel tiles, then stream-K over the rest
+    int32_t dp_tiles;           // stream-K schedule: tiles done whole by one CTA each
+    int64_t sk_kblocks;         // stream-K schedule: k-blocks shared out over the grid
+    int32_t max_seg;            // workspace slots per split tile
     int32_t group;
     int32_t vec_store;          // C rows are 16-byte aligned: float4 stores allowed
     int32_t tma_store;          // epilogue writes C through the TMA store map
@@ -141,6 +146,87 @@ __device__ __forceinline__ void unit_coords(const TcArgs& a, int u, int& pb, int
     pb = first_p + r % gsz;
     qb = r / gsz;
 }
+
+// Tile -> (tile along MMA M side, tile along MMA N side), same raster as
+// unit_coords.
+__device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& pb, int& qb) {
+    const int group_tiles = a.group * a.tiles_q;
+    const int g = tile / group_tiles;
+    const int first_p = g * a.group;
+    const int gsz = min(a.tiles_p - first_p, a.group);
+    const int r = tile - g * group_tiles;
+    pb = first_p + r % gsz;
+    qb = r / gsz;
+}
+
+// One piece of work for a CTA: k-blocks [kb0, kb1) of `tile`.  A tile cut
+// into nseg > 1 pieces has its partial sums stored in workspace slot
+// (slot, seg) and summed in seg order by whichever piece finishes last.
+struct WorkItem {
+    int tile, kb0, kb1, seg, nseg, slot;
+};
+
+// The CTA covering k-block x of the stream-K range (each CTA c owns
+// [c*W/G, (c+1)*W/G)).
+__device__ __forceinline__ int sk_owner(int64_t x, int64_t W, int G) {
+    return static_cast<int>(((x + 1) * G - 1) / W);
+}
+
+// The sequence of work items of one CTA; the producer, the MMA thread and the
+// epilogue each walk the same sequence.
+//   split schedule: unit u = cta, cta + G, ... of tiles x splits equal slices;
+//   stream-K schedule: whole tiles cta, cta + G, ... below dp_tiles, then a
+//   contiguous share of the remaining tiles' k-blocks, cut at tile edges.
+struct WorkIter {
+    int cta, G;
+    int next_u;
+    int64_t pos, end;
+
+    __device__ __forceinline__ WorkIter(const TcArgs& a, int cta_, int G_) : cta(cta_), G(G_), next_u(cta_) {
+        pos = a.sk_kblocks > 0 ? static_cast<int64_t>(cta) * a.sk_kblocks / G : 0;
+        end = a.sk_kblocks > 0 ? static_cast<int64_t>(cta + 1) * a.sk_kblocks / G : 0;
+    }
+
+    __device__ __forceinline__ bool next(const TcArgs& a, WorkItem& it) {
+        if (!a.sk_mode) {
+            if (next_u >= a.num_units) return false;
+            const int u = next_u;
+            next_u += G;
+            it.tile = u / a.splits;
+            it.seg = u - it.tile * a.splits;
+            it.kb0 = it.seg * a.kb_per_split;
+            it.kb1 = min(it.kb0 + a.kb_per_split, a.kb_total);
+            it.nseg = a.splits;
+            it.slot = it.tile;
+            return true;
+        }
+        if (next_u < a.dp_tiles) {
+            it.tile = next_u;
+            next_u += G;
+            it.kb0 = 0;
+            it.kb1 = a.kb_total;
+            it.seg = 0;
+            it.nseg = 1;
+            it.slot = 0;
+            return true;
+        }
+        if (pos >= end) return false;
+        const int64_t KB = a.kb_total;
+        const int64_t ts = pos / KB;
+        const int64_t tile_end = (ts + 1) * KB;
+        const int64_t stop = end < tile_end ? end : tile_end;
+        it.tile = a.dp_tiles + static_cast<int>(ts);
+        it.kb0 = static_cast<int>(pos - ts * KB);
+        it.kb1 = it.kb0 + static_cast<int>(stop - pos);
+        const int first = sk_owner(ts * KB, a.sk_kblocks, G);
+        const int last = sk_owner(tile_end - 1, a.sk_kblocks, G);
+        it.seg = cta - first;
+        it.nseg = last - first + 1;
+        it.slot = static_cast<int>(ts);
+        pos = stop;
+        return true;
+    }
+};
 
 // ---- epilogue stores ----------------------------------------------------------
 
@@ -279,13 +365,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;   // per-stage: armed at least once / parity
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < args.num_units; u += gridDim.x) {
-                int pb, qb, split;
-                unit_coords(args, u, pb, qb, split);
-                const int kb0 = split * args.kb_per_split;
-                const int kb1 = min(kb0 + args.kb_per_split, args.kb_total);
+            WorkIter wi(args, blockIdx.x, gridDim.x);
+            WorkItem it;
+            while (ok && wi.next(args, it)) {
+                int pb, qb;
+                tile_coords(args, it.tile, pb, qb);
                 const int p0 = pb * kTcBM, q0 = qb * BN;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, wctx, kErrProducer)) {
                         ok = false;
                         break;
@@ -326,11 +412,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < args.num_units; u += gridDim.x) {
-                int pb, qb, split;
-                unit_coords(args, u, pb, qb, split);
-                const int kb0 = split * args.kb_per_split;
-                const int kb1 = min(kb0 + args.kb_per_split, args.kb_total);
+            WorkIter wi(args, blockIdx.x, gridDim.x);
+            WorkItem it;
+            while (ok && wi.next(args, it)) {
+                const int kb0 = it.kb0, kb1 = it.kb1;
                 if (!wait_phase(acce_bar(acc), acc_phase ^ 1u, wctx, kErrMma)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -378,9 +463,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
         const bool tma_out = !SWAP && args.tma_store;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < args.num_units; u += gridDim.x) {
-            int pb, qb, split;
-            unit_coords(args, u, pb, qb, split);
+        WorkIter wi(args, blockIdx.x, gridDim.x);
+        WorkItem it;
+        while (wi.next(args, it)) {
+            int pb, qb;
+            tile_coords(args, it.tile, pb, qb);
             bool ok = wait_phase(accf_bar(acc), acc_phase, wctx, kErrEpilogue);
             if (!__all_sync(0xffffffffu, ok)) {
                 *abort_flag = 1;
@@ -391,9 +478,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                                     (static_cast<uint32_t>(quarter * 32) << 16);
             const int p = pb * kTcBM + row;
             const int q0 = qb * BN;
-            const int tile = u / args.splits;
-            float* slot = (args.splits > 1)
-                ? args.ws + (static_cast<int64_t>(tile) * args.splits + split) * (kTcBM * BN)
+            const bool partial = it.nseg > 1;
+            float* slot = partial
+                ? args.ws + (static_cast<int64_t>(it.slot) * args.max_seg + it.seg) * (kTcBM * BN)
                 : nullptr;
 #pragma unroll 1
             for (int c = 0; c < BN / CW; ++c) {
@@ -409,7 +496,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                 float v[CW];
 #pragma unroll
                 for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
-                if (args.splits == 1) {
+                if (!partial) {
                     if constexpr (!SWAP) {
                         if (tma_out) {
                             stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
@@ -425,25 +512,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     for (int i = 0; i < CW; ++i) slot[(c * CW + i) * kTcBM + row] = v[i];
                 }
             }
-            if (args.splits > 1) {
+            if (partial) {
                 __threadfence();
                 __syncwarp();
                 uint32_t last = 0;
                 if (lane == 0) {
-                    uint32_t* cnt = args.counters + tile * 4 + quarter;
-                    last = (atomicAdd(cnt, 1u) == static_cast<uint32_t>(args.splits - 1)) ? 1u : 0u;
+                    uint32_t* cnt = args.counters + it.slot * 4 + quarter;
+                    last = (atomicAdd(cnt, 1u) == static_cast<uint32_t>(it.nseg - 1)) ? 1u : 0u;
                     if (last) atomicExch(cnt, 0u);   // ready for the next launch
                 }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    const float* base = args.ws + static_cast<int64_t>(tile) * args.splits * (kTcBM * BN);
+                    const float* base = args.ws + static_cast<int64_t>(it.slot) * args.max_seg * (kTcBM * BN);
 #pragma unroll 1
                     for (int c = 0; c < BN / CW; ++c) {
                         float v[CW];
 #pragma unroll
                         for (int i = 0; i < CW; ++i) v[i] = 0.0f;
-                        for (int s = 0; s < args.splits; ++s) {
+                        for (int s = 0; s < it.nseg; ++s) {
                             const float* src = base + static_cast<int64_t>(s) * (kTcBM * BN);
 #pragma unroll
                             for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
@@ -782,6 +869,29 @@ cudaError_t watchdog_selftest_launch(uint64_t limit_ns, cudaStream_t stream) {
 
 // ---- host side --------------------------------------------------------------------
 
+int64_t tc_streamk_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sms) {
+    int64_t G = sms;
+    int64_t dp = 0;
+    if (tiles >= G) dp = (tiles % G == 0) ? tiles : (tiles / G - 1) * G;
+    int64_t W = (tiles - dp) * kb_total;
+    if (W > 0 && W < G) G = W;            // every CTA gets at least one k-block
+    if (dp > 0 && W == 0) G = std::min<int64_t>(G, tiles);
+    L.sk_mode = 1;
+    L.dp_tiles = static_cast<int>(dp);
+    L.sk_kblocks = W;
+    L.grid = static_cast<int>(std::max<int64_t>(G, 1));
+    int max_seg = 1;
+    const int64_t sk_tiles = tiles - dp;
+    for (int64_t ts = 0; ts < sk_tiles; ++ts) {
+        const int64_t first = ((ts * kb_total + 1) * G - 1) / W;
+        const int64_t last = (((ts + 1) * kb_total) * G - 1) / W;
+        max_seg = std::max<int>(max_seg, static_cast<int>(last - first + 1));
+    }
+    L.max_seg = max_seg;
+    L.splits = 1;
+    return max_seg > 1 ? sk_tiles : 0;
+}
+
 bool tc_config_supported(int bn, int swap, int pair) {
     if (pair) return !swap && (bn == 128 || bn == 256);
     if (swap) return bn == 16 || bn == 32 || bn == 64;
@@ -891,6 +1001,11 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.splits = L.splits;
     a.kb_per_split = static_cast<int32_t>(ceil_div(a.kb_total, L.splits));
     a.num_units = a.tiles_p * a.tiles_q * L.splits;
+    a.sk_mode = L.sk_mode;
+    a.dp_tiles = L.dp_tiles;
+    a.sk_kblocks = L.sk_kblocks;
+    a.max_seg = L.sk_mode ? L.max_seg : L.splits;
+    if (L.pair && L.sk_mode) return cudaErrorInvalidValue;
     a.group = L.group;
     a.vec_store = ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0 && (L.ldc & 3) == 0) ? 1 : 0;
     // C through TMA stores: FP32 {N, M}, row stride ldc * 4 bytes, box 32 x 32,

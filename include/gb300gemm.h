@@ -119,6 +119,11 @@ gemm_status_t sgemm_f32(const float *A, const float *B, float *C,
  *             256, no swap, no split-K).
  *   store_mode 0 = planner (tensor-core results leave through TMA stores
  *             when C's base, ldc and N allow it), 1 = plain stores.
+ *   stream_k  one-CTA tensor-core kernel: 0 = planner (currently off),
+ *             1 = off, 2 = on.  Stream-K keeps
+ *             whole tiles while whole waves last and shares the remaining
+ *             tiles' k-blocks evenly over all CTAs; a tile cut into pieces
+ *             is summed in a fixed order.  Ignored with split_k > 0.
  * Invalid combinations return GEMM_ERR_INVALID_VALUE.
  */
 typedef struct {
@@ -130,6 +135,8 @@ typedef struct {
     int32_t group_m;
     int32_t cta_pair;
     int32_t store_mode;
+    int32_t stream_k;
+    int32_t reserved[3];
 } gemm_options_t;
 
 /* gemm_ex -- the same operation with an explicit plan (tests and tuning). */

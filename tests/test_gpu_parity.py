@@ -49,6 +49,9 @@ TC_CONFIGS = [
     dict(tile_n=256, swap_ab=0, split_k=1, group_m=3),
     dict(cta_pair=2, tile_n=256), dict(cta_pair=2, tile_n=128),
     dict(cta_pair=2, tile_n=256, group_m=1), dict(cta_pair=1, tile_n=256),
+    dict(cta_pair=1, stream_k=2, tile_n=256), dict(cta_pair=1, stream_k=2, tile_n=64),
+    dict(stream_k=2, tile_n=16, swap_ab=1), dict(stream_k=2, tile_n=64, swap_ab=1),
+    dict(cta_pair=1, stream_k=1, tile_n=128),
 ]
 
 
@@ -227,7 +230,8 @@ def test_golden_fixtures_on_gpu():
 # ---- determinism, streams, host buffers --------------------------------------------
 
 @pytest.mark.parametrize("cfg", [dict(), dict(tile_n=64, swap_ab=1, split_k=6),
-                                 dict(tile_n=128, swap_ab=0, split_k=5)], ids=_cfg_id)
+                                 dict(tile_n=128, swap_ab=0, split_k=5),
+                                 dict(cta_pair=1, tile_n=128, stream_k=2)], ids=_cfg_id)
 def test_repeat_runs_bit_identical(cfg):
     A, B = gu.make_inputs("bf16", "normal", 96, 1000, 2048, 11)
     Cs = [gu.run_gpu("bf16", A, B, 96, 1000, 2048, **cfg) for _ in range(4)]
@@ -281,7 +285,9 @@ def test_cta_pair_kernel(dt, shape):
 MULTI_TILE_PLANS = [dict(cta_pair=1, tile_n=256), dict(cta_pair=1, tile_n=128),
                     dict(cta_pair=1, tile_n=64), dict(cta_pair=2, tile_n=256),
                     dict(cta_pair=2, tile_n=128), dict(cta_pair=1, tile_n=256, store_mode=1),
-                    dict(cta_pair=2, tile_n=256, store_mode=1)]
+                    dict(cta_pair=2, tile_n=256, store_mode=1),
+                    dict(cta_pair=1, tile_n=256, stream_k=2), dict(cta_pair=1, tile_n=128, stream_k=2),
+                    dict(cta_pair=1, tile_n=256, stream_k=2, store_mode=1)]
 
 
 @pytest.mark.parametrize("cfg", MULTI_TILE_PLANS, ids=_cfg_id)
