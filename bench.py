@@ -90,6 +90,24 @@ def kernel_name(plan: str) -> str:
     return "tc_gemm_kernel<256,false> (one CTA, 128x256 tiles)"
 
 
+# ---- multi-rank aggregation ------------------------------------------------------
+
+def max_over_ranks(ms: float, dist=None, device="cpu") -> float:
+    """The slowest rank's timed-region length (every rank gets it)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flop_per_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step, so
+    the job did world x steps steps in the slowest rank's time."""
+    return world * flop_per_step * steps / (max_ms / 1e3) / 1e12
+
+
 # ---- clocks ---------------------------------------------------------------
 
 class ClockSampler:
@@ -281,12 +299,8 @@ def run_gb300(args, rank, world, local_rank):
     g.gemm_device_error(sh)
 
     per = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
-    total_ms = evs[0].elapsed_time(evs[-1])
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * FLOP * args.steps / (total_ms / 1e3) / 1e12
+    total_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dist, device="cuda")
+    value = job_tflops(world, FLOP, args.steps, total_ms)
     kernel_ms = statistics.mean(per)
     peaks = load_peaks()
     achieved = FLOP / (kernel_ms / 1e3) / 1e12
@@ -322,8 +336,8 @@ def run_gb300(args, rank, world, local_rank):
     stream.synchronize()
     g.gemm_device_error(sh)
     e2e_launches = g.gemm_launch_count() - launches_e2e0
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_value = world * FLOP * e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, device="cuda")
+    e2e_value = job_tflops(world, FLOP, e2e_steps, e2e_ms)
     e2e = {"value": e2e_value, "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2),
            "d2h_bytes_per_step": int(Ch.numel() * 4), "steps": e2e_steps,
