@@ -41,7 +41,8 @@ from dataclasses import dataclass
 import numpy as np
 
 __all__ = [
-    "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows",
+    "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows", "gemm_general",
+    "general_bounds",
     "gemm_entries", "compare", "Comparison", "ABS_COEF", "REL_FROB",
 ]
 
@@ -106,6 +107,10 @@ def lib() -> ctypes.CDLL:
                                               i64, ctypes.POINTER(ctypes.c_int64),
                                               ctypes.POINTER(ctypes.c_int64), dp]
             L.oracle_gemm_entries.restype = ctypes.c_int
+            L.oracle_gemm_general.argtypes = [ctypes.c_int, vp, vp, ctypes.POINTER(ctypes.c_float),
+                                              ctypes.c_double, ctypes.c_double, dp, i64, i64, i64,
+                                              i64, i64, i64, ctypes.c_int]
+            L.oracle_gemm_general.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -179,6 +184,36 @@ def gemm(dtype, A, B, M=None, N=None, K=None, lda=None, ldb=None,
     if rc != 0:
         raise RuntimeError(f"oracle_gemm failed ({rc})")
     return C
+
+
+def gemm_general(dtype, A, B, C_in, alpha: float, beta: float, M=None, N=None, K=None,
+                 lda=None, ldb=None, ldc_in=None, nthreads: int | None = None) -> np.ndarray:
+    """alpha * (A x B) + beta * C_in (float64, M x N).  C_in is a float32
+    array of M rows with row stride ldc_in (its own width by default); it is
+    not read when beta == 0.  alpha and beta should be the FP32 values the
+    kernels use (they are widened to double here)."""
+    code = _dtype_code(dtype)
+    A, B = _bits(A, code), _bits(B, code)
+    M, N, K, lda, ldb = _shape_args(A, B, M, N, K, lda, ldb)
+    Ci = np.ascontiguousarray(C_in, dtype=np.float32)
+    ldc_in = Ci.shape[1] if ldc_in is None else ldc_in
+    out = np.empty((M, N), dtype=np.float64)
+    nt = nthreads or os.cpu_count() or 1
+    rc = lib().oracle_gemm_general(code, _ptr(A), _ptr(B),
+                                   Ci.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                   float(alpha), float(beta), _dptr(out), M, N, K, lda, ldb,
+                                   ldc_in, nt)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_general failed ({rc})")
+    return out
+
+
+def general_bounds(K: int, max_abs_a: float, max_abs_b: float, alpha: float, beta: float,
+                   max_abs_c: float) -> float:
+    """Absolute tolerance for alpha * AB + beta * C: the product's bound scaled
+    by |alpha|, plus a few FP32 rounding steps of |beta * C| and of the sum."""
+    prod = ABS_COEF * math.sqrt(K) * max_abs_a * max_abs_b
+    return abs(alpha) * prod + (abs(beta) * max_abs_c + abs(alpha) * K * max_abs_a * max_abs_b) * 2.0 ** -21
 
 
 def gemm_rows(dtype, A, B, row0: int, row1: int, M=None, N=None, K=None,

@@ -266,3 +266,35 @@ int oracle_gemm_entries(int dtype, const void *A, const void *B,
     }
     return 0;
 }
+
+/* ---- the general form: C_out = alpha * (A x B) + beta * C_in ------------- */
+
+/*
+ * The tensor-core operation on the pages accumulates onto an existing matrix
+ * ("04-wmma-matmul" code example, header comment: D = A*B + C on tiles;
+ * "Tensor cores and matrix operations", the pseudocode's accumulator D_tile).
+ * This is that operation with scalars: C_out[i][j] = alpha * sum_k
+ * A[i][k] B[k][j] + beta * C_in[i][j], in double.  C_in is FP32 (row stride
+ * ldc_in) and is not read at all when beta == 0, so whatever it holds (even
+ * NaN) does not reach the result.  C_out is double with row stride N.
+ * Returns 0, -1 on bad arguments, -2 when out of memory.
+ */
+int oracle_gemm_general(int dtype, const void *A, const void *B, const float *C_in,
+                        double alpha, double beta, double *C_out,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc_in, int nthreads)
+{
+    if (ldc_in < N || (beta != 0.0 && C_in == NULL && M > 0 && N > 0))
+        return -1;
+    int rc = oracle_gemm(dtype, A, B, C_out, M, N, K, lda, ldb, N, nthreads);
+    if (rc != 0)
+        return rc;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double v = alpha * C_out[i * N + j];
+            if (beta != 0.0)
+                v += beta * (double)C_in[i * ldc_in + j];
+            C_out[i * N + j] = v;
+        }
+    return 0;
+}
