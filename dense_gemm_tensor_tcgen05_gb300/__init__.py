@@ -65,7 +65,8 @@ class GemmOptions(ctypes.Structure):
                 ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
                 ("generic", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("store_mode", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("stream_k", ctypes.c_int32), ("alpha", ctypes.c_float),
+                ("beta", ctypes.c_float), ("epilogue", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -142,11 +143,16 @@ def sgemm_f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int
 
 
 def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0,
-             cta_pair=0, store_mode=0, stream_k=0) -> GemmOptions:
+             cta_pair=0, store_mode=0, stream_k=0, alpha=None, beta=None) -> GemmOptions:
     o = GemmOptions()
     o.dtype, o.tile_n, o.split_k, o.swap_ab, o.generic, o.group_m = (
         dtype, tile_n, split_k, swap_ab, generic, group_m)
     o.cta_pair, o.store_mode, o.stream_k = cta_pair, store_mode, stream_k
+    if alpha is not None or beta is not None:
+        # C = alpha * (A x B) + beta * C
+        o.epilogue = 1
+        o.alpha = 1.0 if alpha is None else float(alpha)
+        o.beta = 0.0 if beta is None else float(beta)
     return o
 
 
@@ -232,7 +238,9 @@ def matmul(A, B, out=None, stream=None, **opts):
     multiplies and copies C back, pipelined over row panels -- and the call
     returns the CPU result after synchronising the stream (pass page-locked
     tensors for overlapped copies).  ``opts`` are gemm_options_t fields
-    (tile_n, split_k, swap_ab, generic, group_m, cta_pair).
+    (tile_n, split_k, swap_ab, generic, group_m, cta_pair, store_mode,
+    stream_k); alpha= and beta= give C = alpha * (A x B) + beta * out, with
+    ``out`` supplying the old C.
     """
     import torch
 

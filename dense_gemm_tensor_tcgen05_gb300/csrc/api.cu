@@ -211,6 +211,8 @@ enum class Kind { Nothing, ZeroFill, Tc, Generic, Sgemm };
 
 struct Plan {
     Kind kind = Kind::Nothing;
+    int ab = 0;              // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
+    float alpha = 1.0f, beta = 0.0f;
     TcLaunch tc{};
     SgemmLaunch sg{};
     int64_t units = 0;
@@ -221,6 +223,12 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         const gemm_options_t& o, int sms, Plan* plan) {
     Plan p;
+    if (o.epilogue < 0 || o.epilogue > 1) return GEMM_ERR_INVALID_VALUE;
+    if (o.epilogue) {
+        p.alpha = o.alpha;
+        p.beta = o.beta;
+        p.ab = (p.beta != 0.0f) ? 2 : (p.alpha != 1.0f ? 1 : 0);
+    }
     if (M == 0 || N == 0) {
         *plan = p;
         return GEMM_OK;
@@ -239,6 +247,9 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
         } else {
             p.kind = Kind::Sgemm;
             SgemmLaunch& S = p.sg;
+            S.ab = p.ab;
+            S.alpha = p.alpha;
+            S.beta = p.beta;
             S.A = static_cast<const float*>(A);
             S.B = static_cast<const float*>(B);
             S.C = C;
@@ -310,6 +321,9 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
         return GEMM_OK;
     }
     TcLaunch& L = p.tc;
+    L.ab = p.ab;
+    L.alpha = p.alpha;
+    L.beta = p.beta;
     L.A = A; L.B = B; L.C = C;
     L.M = M; L.N = N; L.K = K; L.lda = lda; L.ldb = ldb; L.ldc = ldc;
     L.fmt = dtype;
@@ -430,9 +444,21 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     return GEMM_OK;
 }
 
+void describe_kernel(const Plan& p, int dtype, char* buf, int n);
+
 void describe(const Plan& p, int dtype, char* buf, int64_t size) {
     if (!buf || size <= 0) return;
     const int n = static_cast<int>(size > INT32_MAX ? INT32_MAX : size);
+    describe_kernel(p, dtype, buf, n);
+    if (p.ab) {
+        const size_t len = strlen(buf);
+        if (static_cast<int64_t>(len) + 1 < n)
+            snprintf(buf + len, n - len, " epilogue=%s alpha=%g beta=%g",
+                     p.ab == 2 ? "alpha*AB+beta*C" : "alpha*AB", p.alpha, p.beta);
+    }
+}
+
+void describe_kernel(const Plan& p, int dtype, char* buf, int n) {
     switch (p.kind) {
         case Kind::Nothing: snprintf(buf, n, "nothing (empty output)"); break;
         case Kind::ZeroFill: snprintf(buf, n, "zero-fill (K == 0)"); break;
@@ -492,9 +518,12 @@ gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, 
     if (st != GEMM_OK) return st;
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;
-        case Kind::ZeroFill: return launch_status(fill_zero_launch(C, M, N, ldc, stream), "fill_zero");
+        case Kind::ZeroFill:   // the empty sum: beta * C, or zeros
+            return launch_status(fill_scale_launch(C, M, N, ldc, p.ab == 2 ? p.beta : 0.0f, stream),
+                                 "fill_scale");
         case Kind::Generic:
-            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, stream),
+            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
+                                                p.beta, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
             if (p.ws_floats) {
@@ -775,9 +804,12 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;
-        case Kind::ZeroFill: return launch_status(fill_zero_launch(C, M, N, ldc, stream), "fill_zero");
+        case Kind::ZeroFill:   // the empty sum: beta * C, or zeros
+            return launch_status(fill_scale_launch(C, M, N, ldc, p.ab == 2 ? p.beta : 0.0f, stream),
+                                 "fill_scale");
         case Kind::Generic:
-            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, stream),
+            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
+                                                p.beta, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
             if (p.ws_floats) {
@@ -967,6 +999,10 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
                 HP_CHECK(cudaStreamWaitEvent(stream, h->e_b, 0), "cudaStreamWaitEvent");
             }
             float* cblk = static_cast<float*>(h->dC[buf]) + c0;
+            if (options->epilogue && options->beta != 0.0f)   // C's old values take part
+                HP_CHECK(cudaMemcpy2DAsync(cblk, N * 4, C + r0 * ldc + c0, ldc * 4, cols * 4, rows,
+                                           cudaMemcpyHostToDevice, stream),
+                         "cudaMemcpy2DAsync(C block in)");
             st = run(dtype, h->dA[buf], static_cast<const char*>(h->dB) + c0 * es, cblk, rows, cols,
                      K, K, N, N, *options, stream);
             if (st != GEMM_OK) return st;

@@ -24,6 +24,8 @@ struct TcLaunch {
     int swap;       // 1: MMA M side runs along N of C (C^T = B^T A^T)
     int pair;       // 1: CTA-pair kernel (clusters of 2, 256 x bn tiles)
     int store_mode;    // 0: TMA stores when C allows them, 1: plain stores
+    int ab;            // 0: C = AB; 1: C = alpha AB; 2: C = alpha AB + beta C
+    float alpha, beta;
     int splits;     // K slices (split schedule)
     int sk_mode;    // 1: stream-K schedule (data-parallel tiles, then shared k-blocks)
     int dp_tiles;   // stream-K: tiles done whole
@@ -87,6 +89,8 @@ struct SgemmLaunch {
     int bm, bn;
     int nparts;
     SgemmPart parts[2];
+    int ab;             // 0: C = AB; 1: C = alpha AB; 2: C = alpha AB + beta C
+    float alpha, beta;
     float* ws;          // >= max over parts of tiles * splits * bm * bn floats (if any splits > 1)
     uint32_t* counters; // >= max over parts of tiles, zero between launches
 };
@@ -97,7 +101,9 @@ int sgemm_k_step();
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                           cudaStream_t stream);
-cudaError_t fill_zero_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream);
+                           int ab, float alpha, float beta, cudaStream_t stream);
+// C = beta * C (scale != 0) or C = 0 (scale == 0, C not read): the K == 0 result.
+cudaError_t fill_scale_launch(float* C, int64_t M, int64_t N, int64_t ldc, float scale,
+                              cudaStream_t stream);
 
 }  // namespace gb300

@@ -57,6 +57,8 @@ struct SgArgs {
     int tile0;          // first (row-major linear) tile of this launch
     int splits;         // K slices per tile; 1 = the whole K
     int k_chunk;        // K per slice, a multiple of BK
+    int ab;             // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
+    float alpha, beta;
     float* ws;          // split-K partial tiles of this launch
     uint32_t* counters; // split-K arrival counter per tile, zero between launches
 };
@@ -196,7 +198,25 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
 #pragma unroll
             for (int qj = 0; qj < 2; ++qj) {
                 const int gn = n0 + qj * (BN / 2) + tx * 4;
-                const float* v = &acc[qi * 4 + i][qj * 4];
+                float v[4] = {acc[qi * 4 + i][qj * 4], acc[qi * 4 + i][qj * 4 + 1],
+                              acc[qi * 4 + i][qj * 4 + 2], acc[qi * 4 + i][qj * 4 + 3]};
+                if (a.ab == 1) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] *= a.alpha;
+                } else if (a.ab == 2) {
+                    // alpha * AB + beta * C, reading C only inside it
+                    if (!EDGE) {
+                        const float4 c = *reinterpret_cast<const float4*>(crow + gn);
+                        v[0] = fmaf(a.alpha, v[0], a.beta * c.x);
+                        v[1] = fmaf(a.alpha, v[1], a.beta * c.y);
+                        v[2] = fmaf(a.alpha, v[2], a.beta * c.z);
+                        v[3] = fmaf(a.alpha, v[3], a.beta * c.w);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            v[j] = fmaf(a.alpha, v[j], (gn + j < a.N) ? a.beta * crow[gn + j] : 0.0f);
+                    }
+                }
                 if (!EDGE) {
                     *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
                 } else {
@@ -307,6 +327,9 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
         a.tile0 = part.tile0;
         a.splits = part.splits;
         a.k_chunk = part.k_chunk;
+        a.ab = L.ab;
+        a.alpha = L.alpha;
+        a.beta = L.beta;
         a.ws = L.ws;
         a.counters = L.counters;
         sgemm_kernel<BM, BN, kSgemmBK>
@@ -334,7 +357,8 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return
 template <typename T>
 __global__ void __launch_bounds__(256)
 generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __restrict__ C,
-                    int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc) {
+                    int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc, int ab, float alpha,
+                    float beta) {
     __shared__ float As[16][64 + 1];
     __shared__ float Bs[16][64 + 1];
     const int tid = threadIdx.x;
@@ -372,17 +396,25 @@ generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __r
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int gn = n0 + tx + 16 * j;
-            if (gn < N) C[static_cast<int64_t>(gm) * ldc + gn] = acc[i][j];
+            if (gn < N) {
+                float* dst = C + static_cast<int64_t>(gm) * ldc + gn;
+                float v = acc[i][j];
+                if (ab == 1) v *= alpha;
+                else if (ab == 2) v = fmaf(alpha, v, beta * *dst);
+                *dst = v;
+            }
         }
     }
 }
 
-__global__ void fill_zero_kernel(float* C, int64_t M, int64_t N, int64_t ldc) {
+// C = scale * C, or C = 0 without reading C when scale == 0.
+__global__ void fill_scale_kernel(float* C, int64_t M, int64_t N, int64_t ldc, float scale) {
     const int64_t total = M * N;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / N, c = i - r * N;
-        C[r * ldc + c] = 0.0f;
+        float* p = C + r * ldc + c;
+        *p = (scale == 0.0f) ? 0.0f : scale * *p;
     }
 }
 
@@ -416,33 +448,36 @@ cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream) {
 
 cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                           cudaStream_t stream) {
+                           int ab, float alpha, float beta, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(ceil_div(N, 64)), static_cast<unsigned>(ceil_div(M, 64)));
     const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
     switch (dtype) {
         case 0:
             generic_gemm_kernel<__half><<<grid, 256, 0, stream>>>(
-                static_cast<const __half*>(A), static_cast<const __half*>(B), C, m, n, k, lda, ldb, ldc);
+                static_cast<const __half*>(A), static_cast<const __half*>(B), C, m, n, k, lda, ldb, ldc,
+                ab, alpha, beta);
             break;
         case 1:
             generic_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
                 static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), C, m, n,
-                k, lda, ldb, ldc);
+                k, lda, ldb, ldc, ab, alpha, beta);
             break;
         default:
             generic_gemm_kernel<float><<<grid, 256, 0, stream>>>(
-                static_cast<const float*>(A), static_cast<const float*>(B), C, m, n, k, lda, ldb, ldc);
+                static_cast<const float*>(A), static_cast<const float*>(B), C, m, n, k, lda, ldb, ldc,
+                ab, alpha, beta);
             break;
     }
     return cudaGetLastError();
 }
 
-cudaError_t fill_zero_launch(float* C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream) {
+cudaError_t fill_scale_launch(float* C, int64_t M, int64_t N, int64_t ldc, float scale,
+                              cudaStream_t stream) {
     const int64_t total = M * N;
     int64_t blocks = ceil_div(total, 256);
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
-    fill_zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc);
+    fill_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc, scale);
     return cudaGetLastError();
 }
 

@@ -75,6 +75,8 @@ struct TcArgs {
     int32_t group;
     int32_t vec_store;          // C rows are 16-byte aligned: float4 stores allowed
     int32_t tma_store;          // epilogue writes C through the TMA store map
+    int32_t ab;                 // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
+    float alpha, beta;
     uint32_t idesc;
     float* ws;
     uint32_t* counters;
@@ -260,6 +262,44 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, const float (&v)[W]
             for (int i = 0; i < W; ++i)
                 if (q0 + i < a.M) dst[static_cast<int64_t>(i) * a.ldc] = v[i];
         }
+    }
+}
+
+// alpha * v + beta * C for W accumulator values of this thread (same
+// coordinates as store_chunk), before they are stored.  C is read only when
+// beta is in play (ab == 2), and only inside C.
+template <bool SWAP, int W>
+__device__ __forceinline__ void apply_ab(const TcArgs& a, float (&v)[W], int p, int q0) {
+    if (!a.ab) return;
+    const float alpha = a.alpha, beta = a.beta;
+    if (a.ab == 1) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] *= alpha;
+        return;
+    }
+    if (!SWAP) {
+        if (p >= a.M) return;   // never stored
+        const float* src = a.C + static_cast<int64_t>(p) * a.ldc + q0;
+        if (a.vec_store && q0 + W <= a.N) {
+#pragma unroll
+            for (int i = 0; i < W; i += 4) {
+                const float4 c = *reinterpret_cast<const float4*>(src + i);
+                v[i] = fmaf(alpha, v[i], beta * c.x);
+                v[i + 1] = fmaf(alpha, v[i + 1], beta * c.y);
+                v[i + 2] = fmaf(alpha, v[i + 2], beta * c.z);
+                v[i + 3] = fmaf(alpha, v[i + 3], beta * c.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i)
+                v[i] = fmaf(alpha, v[i], (q0 + i < a.N) ? beta * src[i] : 0.0f);
+        }
+    } else {
+        if (p >= a.N) return;
+        const float* src = a.C + static_cast<int64_t>(q0) * a.ldc + p;
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            v[i] = fmaf(alpha, v[i], (q0 + i < a.M) ? beta * src[static_cast<int64_t>(i) * a.ldc] : 0.0f);
     }
 }
 
@@ -497,6 +537,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
 #pragma unroll
                 for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
                 if (!partial) {
+                    apply_ab<SWAP, CW>(args, v, p, q0 + c * CW);
                     if constexpr (!SWAP) {
                         if (tma_out) {
                             stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
@@ -535,6 +576,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
 #pragma unroll
                             for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
                         }
+                        apply_ab<SWAP, CW>(args, v, p, q0 + c * CW);
                         if constexpr (!SWAP) {
                             if (tma_out) {
                                 stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
@@ -800,6 +842,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 float v[CW];
 #pragma unroll
                 for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+                apply_ab<false, CW>(args, v, p, q0 + c * CW);
                 if (args.tma_store)
                     stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
                                     pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM + quarter * 32,
@@ -1031,6 +1074,9 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
                             L.pair ? 2 * kTcBM : kTcBM, static_cast<uint32_t>(L.bn));
     a.ws = L.ws;
     a.counters = L.counters;
+    a.ab = L.ab;
+    a.alpha = L.alpha;
+    a.beta = L.beta;
 
     const CUtensorMap& mp = L.swap ? map_b : map_a;
     const CUtensorMap& mq = L.swap ? map_a : map_b;

@@ -120,7 +120,13 @@ gemm_status_t sgemm_f32(const float *A, const float *B, float *C,
  *   store_mode 0 = planner (tensor-core results leave through TMA stores
  *             when C's base, ldc and N allow it), 1 = plain stores.
  *   stream_k  one-CTA tensor-core kernel: 0 = planner (currently off),
- *             1 = off, 2 = on.  Stream-K keeps
+ *             1 = off, 2 = on.
+ *   epilogue  0 = C = A x B (alpha and beta ignored); 1 = C = alpha * (A x B)
+ *             + beta * C, the accumulate-onto-C form of the tensor-core
+ *             operation ("04-wmma-matmul", header comment: D = A*B + C).  The
+ *             product is accumulated in FP32, then scaled and added in FP32.
+ *             With beta == 0, C is not read (it may hold anything, NaN
+ *             included).  With K == 0 the result is beta * C.  Stream-K keeps
  *             whole tiles while whole waves last and shares the remaining
  *             tiles' k-blocks evenly over all CTAs; a tile cut into pieces
  *             is summed in a fixed order.  Ignored with split_k > 0.
@@ -136,7 +142,9 @@ typedef struct {
     int32_t cta_pair;
     int32_t store_mode;
     int32_t stream_k;
-    int32_t reserved[3];
+    float alpha;
+    float beta;
+    int32_t epilogue;
 } gemm_options_t;
 
 /* gemm_ex -- the same operation with an explicit plan (tests and tuning). */
@@ -191,6 +199,8 @@ gemm_status_t gemm_release_workspace(void);
  * `stream`) and copies each C block back as soon as it is done, on two
  * internal copy streams, so the two copy directions overlap each other and
  * the products.
+ * With epilogue 1 and beta != 0, each C block is also copied in before its
+ * product (on `stream`).
  * For the copies to overlap, A, B and C must be page-locked (cudaHostAlloc /
  * cudaHostRegister); pageable memory works but serialises.  Leading
  * dimensions are those of the host arrays.

@@ -33,7 +33,7 @@ def to_device(bits: np.ndarray, dt: str, offset_elems: int = 0):
 
 
 def run_gpu(dt, A_bits, B_bits, M, N, K, lda=None, ldb=None, ldc=None, offsets=(0, 0, 0),
-            stream=None, **opts):
+            stream=None, c_init=None, **opts):
     """C (M x N float32 numpy) from the library.  C starts as NaN everywhere,
     so an unwritten element fails any comparison, and padding columns of C
     (ldc > N) must still be NaN afterwards."""
@@ -49,6 +49,8 @@ def run_gpu(dt, A_bits, B_bits, M, N, K, lda=None, ldb=None, ldc=None, offsets=(
     cbuf = torch.full((rows * ldc + offsets[2] + guard,), float("nan"), dtype=torch.float32,
                       device="cuda")
     Cd = cbuf[offsets[2]:]
+    if c_init is not None:   # C's old values (M x ldc), for C = alpha AB + beta C
+        Cd[: M * ldc].copy_(torch.from_numpy(np.ascontiguousarray(c_init, dtype=np.float32).ravel()))
     st = stream if stream is not None else torch.cuda.current_stream()
     sh = st.cuda_stream
     args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), M, N, K, lda, ldb, ldc)
@@ -64,7 +66,11 @@ def run_gpu(dt, A_bits, B_bits, M, N, K, lda=None, ldb=None, ldc=None, offsets=(
         assert torch.isnan(cbuf[:offsets[2]]).all().item(), "kernel wrote before the start of C"
     C = Cd[: rows * ldc].reshape(rows, ldc).cpu().numpy()[:M]
     if ldc > N and M > 0:
-        assert np.all(np.isnan(C[:, N:])), "kernel wrote into C's padding columns"
+        if c_init is None:
+            assert np.all(np.isnan(C[:, N:])), "kernel wrote into C's padding columns"
+        else:
+            assert np.array_equal(C[:, N:], c_init[:, N:], equal_nan=True), \
+                "kernel wrote into C's padding columns"
     return C[:, :N]
 
 
