@@ -41,7 +41,7 @@ from dataclasses import dataclass
 import numpy as np
 
 __all__ = [
-    "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows", "gemm_general",
+    "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows", "gemm_general", "gemm_op",
     "general_bounds",
     "gemm_entries", "compare", "Comparison", "ABS_COEF", "REL_FROB",
 ]
@@ -111,6 +111,9 @@ def lib() -> ctypes.CDLL:
                                               ctypes.c_double, ctypes.c_double, dp, i64, i64, i64,
                                               i64, i64, i64, ctypes.c_int]
             L.oracle_gemm_general.restype = ctypes.c_int
+            L.oracle_gemm_op.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, dp,
+                                         i64, i64, i64, i64, i64, i64, ctypes.c_int]
+            L.oracle_gemm_op.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -206,6 +209,26 @@ def gemm_general(dtype, A, B, C_in, alpha: float, beta: float, M=None, N=None, K
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_general failed ({rc})")
     return out
+
+
+def gemm_op(dtype, trans_a: bool, trans_b: bool, A, B, M: int, N: int, K: int,
+            lda: int | None = None, ldb: int | None = None,
+            nthreads: int | None = None) -> np.ndarray:
+    """op(A) x op(B) (float64, M x N).  A holds op(A) row-major (M x K) when
+    trans_a is false and its transpose row-major (K x M) when true; B
+    likewise (K x N, or N x K when trans_b).  Leading dimensions default to
+    the arrays' widths."""
+    code = _dtype_code(dtype)
+    A, B = _bits(A, code), _bits(B, code)
+    lda = A.shape[1] if lda is None else lda
+    ldb = B.shape[1] if ldb is None else ldb
+    C = np.empty((M, N), dtype=np.float64)
+    nt = nthreads or os.cpu_count() or 1
+    rc = lib().oracle_gemm_op(code, int(bool(trans_a)), int(bool(trans_b)), _ptr(A), _ptr(B),
+                              _dptr(C), M, N, K, lda, ldb, N, nt)
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_op failed ({rc})")
+    return C
 
 
 def general_bounds(K: int, max_abs_a: float, max_abs_b: float, alpha: float, beta: float,

@@ -298,3 +298,83 @@ int oracle_gemm_general(int dtype, const void *A, const void *B, const float *C_
         }
     return 0;
 }
+
+/* ---- transposed operands: C = op(A) x op(B) ------------------------------- */
+
+/*
+ * op(A) is M x K and op(B) is K x N.  trans_a == 0: A is stored as op(A),
+ * row-major M x K (element (i, k) at A[i*lda + k], lda >= K); trans_a == 1: A
+ * is stored as its transpose, row-major K x M (element (i, k) of op(A) at
+ * A[k*lda + i], lda >= M).  Likewise trans_b == 0: B row-major K x N (ldb >=
+ * N); trans_b == 1: B stored N x K (element (k, j) at B[j*ldb + k], ldb >=
+ * K).  This is the row-major reading of the column-major trick the
+ * "matmul_registers.cu" lesson uses with cuBLAS (a row-major matrix is the
+ * column-major storage of its transpose).  The product is then the plain
+ * definition, summed in double in increasing k.  C_out is row-major with
+ * stride ldc.  Returns 0, -1 on bad arguments, -2 when out of memory.
+ */
+int oracle_gemm_op(int dtype, int trans_a, int trans_b, const void *A, const void *B,
+                   double *C, int64_t M, int64_t N, int64_t K,
+                   int64_t lda, int64_t ldb, int64_t ldc, int nthreads)
+{
+    if (dtype < ORACLE_F16 || dtype > ORACLE_F32)
+        return -1;
+    if (M < 0 || N < 0 || K < 0 || ldc < N)
+        return -1;
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N))
+        return -1;
+    if (M == 0 || N == 0)
+        return 0;
+    double *a = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    double *b = (double *)malloc(sizeof(double) * (size_t)(K * N > 0 ? K * N : 1));
+    if (!a || !b) {
+        free(a);
+        free(b);
+        return -2;
+    }
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t p = 0; p < K; ++p)
+            a[i * K + p] = decode_one(dtype, A, trans_a ? p * lda + i : i * lda + p);
+    for (int64_t p = 0; p < K; ++p)
+        for (int64_t j = 0; j < N; ++j)
+            b[p * N + j] = decode_one(dtype, B, trans_b ? j * ldb + p : p * ldb + j);
+
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > M)
+        nthreads = (int)M;
+    rows_job *jobs = (rows_job *)malloc(sizeof(rows_job) * (size_t)nthreads);
+    pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!jobs || !tids) {
+        free(a); free(b); free(jobs); free(tids);
+        return -2;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].a = a;
+        jobs[t].b = b;
+        jobs[t].c = C;
+        jobs[t].n = N;
+        jobs[t].k = K;
+        jobs[t].lda = K;
+        jobs[t].ldc = ldc;
+        jobs[t].row0 = 0;
+        jobs[t].row_begin = M * t / nthreads;
+        jobs[t].row_end = M * (t + 1) / nthreads;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, rows_worker, &jobs[t]) != 0)
+            break;
+        ++started;
+    }
+    rows_worker(&jobs[0]);
+    for (int t = 1; t <= started; ++t)
+        pthread_join(tids[t], NULL);
+    for (int t = started + 1; t < nthreads; ++t)
+        rows_worker(&jobs[t]);
+    free(jobs);
+    free(tids);
+    free(a);
+    free(b);
+    return 0;
+}
