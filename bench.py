@@ -375,29 +375,47 @@ def run_gb300(args, rank, world, local_rank):
 def run_suite(g, torch, np, peaks):
     """Every workload configuration, timed (not part of the JSON line)."""
     from dense_gemm_tensor_tcgen05_gb300 import inputs
-    cfgs = [("f16", "uniform", 1024, 1024, 1024, 1.0), ("f32", "uniform", 1024, 1024, 1024, 1.0),
-            ("f32", "uniform", 4096, 4096, 4096, 1.0), ("f16", "normal", 2048, 2048, 2048, 1.0),
-            ("bf16", "normal", 8192, 8192, 8192, 1 / math.sqrt(8192)),
-            ("f16", "uniform", 4000, 3000, 1000, 1.0), ("f16", "uniform", 16384, 128, 4096, 1.0),
-            ("f16", "uniform", 8, 8192, 8192, 1.0)]
+    sig = 1 / math.sqrt(8192)
+    # (dtype, dist, M, N, K, sigma, options): the workload configurations, then
+    # the headline shape under the extended operations (alpha/beta epilogue,
+    # transposed storage of A and/or B)
+    cfgs = [("f16", "uniform", 1024, 1024, 1024, 1.0, {}), ("f32", "uniform", 1024, 1024, 1024, 1.0, {}),
+            ("f32", "uniform", 4096, 4096, 4096, 1.0, {}), ("f16", "normal", 2048, 2048, 2048, 1.0, {}),
+            ("bf16", "normal", 8192, 8192, 8192, sig, {}),
+            ("f16", "uniform", 4000, 3000, 1000, 1.0, {}), ("f16", "uniform", 16384, 128, 4096, 1.0, {}),
+            ("f16", "uniform", 8, 8192, 8192, 1.0, {}),
+            ("bf16", "normal", 8192, 8192, 8192, sig, dict(alpha=0.5, beta=1.0)),
+            ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_a=1)),
+            ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
+            ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_a=1, trans_b=1))]
     fns = {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32}
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     out = []
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    for dt, dist, m, n, k, sigma in cfgs:
+    for dt, dist, m, n, k, sigma, opts in cfgs:
         A = inputs.make(dist, dt, m, k, 1, 0, sigma)
         B = inputs.make(dist, dt, k, n, 1, 1, sigma)
+        ta, tb = opts.get("trans_a", 0), opts.get("trans_b", 0)
+        if ta:
+            A = np.ascontiguousarray(A.T)     # stored K x M
+        if tb:
+            B = np.ascontiguousarray(B.T)     # stored N x K
         if dt == "f32":
             Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
         else:
             Ad = torch.from_numpy(A.view(np.int16)).view(tdt[dt]).cuda()
             Bd = torch.from_numpy(B.view(np.int16)).view(tdt[dt]).cuda()
-        Cd = torch.empty((m, n), dtype=torch.float32, device="cuda")
-        call = lambda: fns[dt](Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), m, n, k, k, n, n, sh)
-        plan = g.gemm_plan_describe({"f16": 0, "bf16": 1, "f32": 2}[dt], Ad.data_ptr(),
-                                    Bd.data_ptr(), Cd.data_ptr(), m, n, k, k, n, n)
+        Cd = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+        code = {"f16": 0, "bf16": 1, "f32": 2}[dt]
+        lda, ldb = (m if ta else k), (k if tb else n)
+        args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), m, n, k, lda, ldb, n)
+        if opts:
+            call = lambda: g.gemm_ex(*args, dtype=code, stream=sh, **opts)
+        else:
+            call = lambda: fns[dt](*args, sh)
+        plan = g.gemm_plan_describe(code, *args, **opts)
         for _ in range(5):
             call()
         torch.cuda.synchronize()
@@ -430,7 +448,9 @@ def run_suite(g, torch, np, peaks):
         g.gemm_device_error(sh)
         flop = 2.0 * m * n * k
         byts = (m * k + k * n) * (4 if dt == "f32" else 2) + m * n * 4
-        out.append({"dtype": dt, "M": m, "N": n, "K": k, "plan": plan,
+        if opts.get("beta"):
+            byts += m * n * 4            # C is read as well
+        out.append({"dtype": dt, "M": m, "N": n, "K": k, "options": opts, "plan": plan,
                     "warm_ms": warm_ms, "cold_ms": cold_ms,
                     "tflops_warm": flop / warm_ms / 1e9, "tflops_cold": flop / cold_ms / 1e9,
                     "gbs_warm": byts / warm_ms / 1e6, "gbs_cold": byts / cold_ms / 1e6,

@@ -66,7 +66,9 @@ class GemmOptions(ctypes.Structure):
                 ("generic", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("cta_pair", ctypes.c_int32), ("store_mode", ctypes.c_int32),
                 ("stream_k", ctypes.c_int32), ("alpha", ctypes.c_float),
-                ("beta", ctypes.c_float), ("epilogue", ctypes.c_int32)]
+                ("beta", ctypes.c_float), ("epilogue", ctypes.c_int32),
+                ("trans_a", ctypes.c_int32), ("trans_b", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lock = threading.Lock()
@@ -143,11 +145,13 @@ def sgemm_f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int
 
 
 def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0,
-             cta_pair=0, store_mode=0, stream_k=0, alpha=None, beta=None) -> GemmOptions:
+             cta_pair=0, store_mode=0, stream_k=0, alpha=None, beta=None, trans_a=0,
+             trans_b=0) -> GemmOptions:
     o = GemmOptions()
     o.dtype, o.tile_n, o.split_k, o.swap_ab, o.generic, o.group_m = (
         dtype, tile_n, split_k, swap_ab, generic, group_m)
     o.cta_pair, o.store_mode, o.stream_k = cta_pair, store_mode, stream_k
+    o.trans_a, o.trans_b = int(bool(trans_a)), int(bool(trans_b))
     if alpha is not None or beta is not None:
         # C = alpha * (A x B) + beta * C
         o.epilogue = 1
@@ -228,6 +232,20 @@ def _row_major_ld(t, name: str) -> int:
     return max(t.stride(0), t.size(1)) if t.size(0) > 1 else max(t.size(1), 1)
 
 
+def _operand_layout(t, name: str):
+    """(transposed, ld) of a 2-D operand: row-major (unit column stride) is
+    stored as itself; column-major (unit row stride, e.g. a .t() view) is the
+    row-major storage of its transpose."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    rows, cols = t.shape
+    if t.stride(1) == 1 or cols <= 1:
+        return 0, _row_major_ld(t, name)
+    if t.stride(0) == 1 or rows <= 1:
+        return 1, max(t.stride(1), rows, 1)
+    raise ValueError(f"{name} must be row-major or column-major")
+
+
 def matmul(A, B, out=None, stream=None, **opts):
     """C = A @ B for 2-D tensors (row-major, any row stride).
 
@@ -269,7 +287,11 @@ def matmul(A, B, out=None, stream=None, **opts):
             out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     elif out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a float32 CUDA tensor of shape (M, N)")
-    lda, ldb, ldc = _row_major_ld(A, "A"), _row_major_ld(B, "B"), _row_major_ld(out, "C")
+    ldc = _row_major_ld(out, "C")
+    ta, lda = _operand_layout(A, "A")
+    tb, ldb = _operand_layout(B, "B")
+    if ta or tb:
+        opts = dict(opts, trans_a=ta, trans_b=tb)
     args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc)
     sh = st.cuda_stream
     if opts:

@@ -181,25 +181,30 @@ bool spans_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
 }
 
 gemm_status_t check_args(const void* A, const void* B, const float* C, int64_t M, int64_t N,
-                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int esize) {
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int esize,
+                         int trans_a = 0, int trans_b = 0) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
-    if (lda < K || ldb < N || ldc < N) return GEMM_ERR_INVALID_VALUE;
+    if (trans_a < 0 || trans_a > 1 || trans_b < 0 || trans_b > 1) return GEMM_ERR_INVALID_VALUE;
+    // stored shapes: A is M x K (or K x M transposed), B is K x N (or N x K)
+    const int64_t a_rows = trans_a ? K : M, a_cols = trans_a ? M : K;
+    const int64_t b_rows = trans_b ? N : K, b_cols = trans_b ? K : N;
+    if (lda < a_cols || ldb < b_cols || ldc < N) return GEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return GEMM_ERR_INVALID_VALUE;
     if (K > 0 && (!A || !B)) return GEMM_ERR_INVALID_VALUE;
     // keep every byte offset well inside int64
     const int64_t lim = INT64_MAX / 16;
-    if ((M > 1 && ldc > lim / (M - 1)) || (M > 1 && lda > lim / (M - 1)) ||
-        (K > 1 && ldb > lim / (K - 1)))
+    if ((M > 1 && ldc > lim / (M - 1)) || (a_rows > 1 && lda > lim / (a_rows - 1)) ||
+        (b_rows > 1 && ldb > lim / (b_rows - 1)))
         return GEMM_ERR_INVALID_VALUE;
     const uintptr_t c0 = reinterpret_cast<uintptr_t>(C);
     const uintptr_t c1 = c0 + static_cast<uintptr_t>((M - 1) * ldc + N) * 4;
     if (K > 0) {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(A);
-        const uintptr_t a1 = a0 + static_cast<uintptr_t>((M - 1) * lda + K) * esize;
+        const uintptr_t a1 = a0 + static_cast<uintptr_t>((a_rows - 1) * lda + a_cols) * esize;
         const uintptr_t b0 = reinterpret_cast<uintptr_t>(B);
-        const uintptr_t b1 = b0 + static_cast<uintptr_t>((K - 1) * ldb + N) * esize;
+        const uintptr_t b1 = b0 + static_cast<uintptr_t>((b_rows - 1) * ldb + b_cols) * esize;
         if (spans_overlap(c0, c1, a0, a1) || spans_overlap(c0, c1, b0, b1)) return GEMM_ERR_OVERLAP;
     }
     return GEMM_OK;
@@ -213,6 +218,7 @@ struct Plan {
     Kind kind = Kind::Nothing;
     int ab = 0;              // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
     float alpha = 1.0f, beta = 0.0f;
+    int trans_a = 0, trans_b = 0;
     TcLaunch tc{};
     SgemmLaunch sg{};
     int64_t units = 0;
@@ -224,6 +230,9 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
                         const gemm_options_t& o, int sms, Plan* plan) {
     Plan p;
     if (o.epilogue < 0 || o.epilogue > 1) return GEMM_ERR_INVALID_VALUE;
+    if (o.trans_a < 0 || o.trans_a > 1 || o.trans_b < 0 || o.trans_b > 1) return GEMM_ERR_INVALID_VALUE;
+    p.trans_a = o.trans_a;
+    p.trans_b = o.trans_b;
     if (o.epilogue) {
         p.alpha = o.alpha;
         p.beta = o.beta;
@@ -242,7 +251,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
         const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
                                reinterpret_cast<uintptr_t>(C)) & 15) == 0 &&
                              (lda & 3) == 0 && (ldb & 3) == 0 && (ldc & 3) == 0;
-        if (o.generic || !aligned) {
+        if (o.generic || !aligned || o.trans_a || o.trans_b) {
             p.kind = Kind::Generic;
         } else {
             p.kind = Kind::Sgemm;
@@ -321,6 +330,8 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
         return GEMM_OK;
     }
     TcLaunch& L = p.tc;
+    L.trans_a = p.trans_a;
+    L.trans_b = p.trans_b;
     L.ab = p.ab;
     L.alpha = p.alpha;
     L.beta = p.beta;
@@ -364,9 +375,12 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     const int64_t qe = L.swap ? M : N;     // extent along the MMA N side
     if (o.tile_n) {
         if (!tc_config_supported(o.tile_n, L.swap, 0)) return GEMM_ERR_INVALID_VALUE;
+        if (L.swap && L.trans_a && o.tile_n % 64) return GEMM_ERR_INVALID_VALUE;
         L.bn = o.tile_n;
     } else if (L.swap) {
-        L.bn = qe <= 16 ? 16 : qe <= 32 ? 32 : 64;
+        // with A stored transposed the swapped B operand (rows of C) is
+        // M-contiguous, loaded in 64-row boxes: BN = 64
+        L.bn = L.trans_a ? 64 : (qe <= 16 ? 16 : qe <= 32 ? 32 : 64);
     } else if (qe <= 64) {
         L.bn = 64;
     } else {
@@ -506,7 +520,7 @@ gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, 
                   cudaStream_t stream) {
     if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
     const int esize = dtype == 2 ? 4 : 2;
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize);
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize, o.trans_a, o.trans_b);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev;
@@ -523,7 +537,7 @@ gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, 
                                  "fill_scale");
         case Kind::Generic:
             return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
-                                                p.beta, stream),
+                                                p.beta, p.trans_a, p.trans_b, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
             if (p.ws_floats) {
@@ -592,13 +606,14 @@ gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, co
                                  int64_t size) {
     if (buf && size > 0) buf[0] = '\0';
     if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2);
+    gemm_options_t o = options ? *options : default_options(dtype);
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2, o.trans_a,
+                                  o.trans_b);
     if (st != GEMM_OK) return st;
     int dev;
     DeviceInfo info;
     st = current_device(&dev, &info);
     if (st != GEMM_OK) return st;
-    gemm_options_t o = options ? *options : default_options(dtype);
     Plan p;
     st = make_plan(dtype, A, B, const_cast<float*>(C), M, N, K, lda, ldb, ldc, o, info.sms, &p);
     if (st == GEMM_OK) describe(p, dtype, buf, size);
@@ -792,7 +807,8 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
     if (!options) return GEMM_ERR_INVALID_VALUE;
     const int dtype = options->dtype;
     if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2);
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2,
+                                  options->trans_a, options->trans_b);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev = 0, sms = 0;
@@ -809,7 +825,7 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
                                  "fill_scale");
         case Kind::Generic:
             return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
-                                                p.beta, stream),
+                                                p.beta, p.trans_a, p.trans_b, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
             if (p.ws_floats) {
@@ -937,6 +953,7 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
     const int dtype = options->dtype;
     if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
     const size_t es = dtype == 2 ? 4 : 2;
+    if (options->trans_a || options->trans_b) return GEMM_ERR_INVALID_VALUE;
     gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es));
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;

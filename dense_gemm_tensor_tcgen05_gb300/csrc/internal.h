@@ -26,6 +26,7 @@ struct TcLaunch {
     int store_mode;    // 0: TMA stores when C allows them, 1: plain stores
     int ab;            // 0: C = AB; 1: C = alpha AB; 2: C = alpha AB + beta C
     float alpha, beta;
+    int trans_a, trans_b;  // A stored K x M / B stored N x K (their transposes)
     int splits;     // K slices (split schedule)
     int sk_mode;    // 1: stream-K schedule (data-parallel tiles, then shared k-blocks)
     int dp_tiles;   // stream-K: tiles done whole
@@ -101,7 +102,8 @@ int sgemm_k_step();
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                           int ab, float alpha, float beta, cudaStream_t stream);
+                           int ab, float alpha, float beta, int trans_a, int trans_b,
+                           cudaStream_t stream);
 // C = beta * C (scale != 0) or C = 0 (scale == 0, C not read): the K == 0 result.
 cudaError_t fill_scale_launch(float* C, int64_t M, int64_t N, int64_t ldc, float scale,
                               cudaStream_t stream);

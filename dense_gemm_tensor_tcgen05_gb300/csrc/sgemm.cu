@@ -358,7 +358,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __restrict__ C,
                     int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc, int ab, float alpha,
-                    float beta) {
+                    float beta, int trans_a, int trans_b) {
     __shared__ float As[16][64 + 1];
     __shared__ float Bs[16][64 + 1];
     const int tid = threadIdx.x;
@@ -369,10 +369,15 @@ generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __r
         for (int l = tid; l < 64 * 16; l += 256) {
             const int r = l / 16, c = l % 16;     // A: 64 rows x 16 k
             const int gm = m0 + r, gk = k0 + c;
-            As[c][r] = (gm < M && gk < K) ? to_f32(A[static_cast<int64_t>(gm) * lda + gk]) : 0.0f;
+            // element (gm, gk) of op(A): A[gm][gk], or A[gk][gm] when A is stored transposed
+            As[c][r] = (gm < M && gk < K)
+                ? to_f32(A[trans_a ? static_cast<int64_t>(gk) * lda + gm : static_cast<int64_t>(gm) * lda + gk])
+                : 0.0f;
             const int kr = l / 64, nc = l % 64;   // B: 16 k x 64 cols
             const int bk = k0 + kr, bn = n0 + nc;
-            Bs[kr][nc] = (bk < K && bn < N) ? to_f32(B[static_cast<int64_t>(bk) * ldb + bn]) : 0.0f;
+            Bs[kr][nc] = (bk < K && bn < N)
+                ? to_f32(B[trans_b ? static_cast<int64_t>(bn) * ldb + bk : static_cast<int64_t>(bk) * ldb + bn])
+                : 0.0f;
         }
         __syncthreads();
 #pragma unroll
@@ -448,24 +453,25 @@ cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream) {
 
 cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                           int ab, float alpha, float beta, cudaStream_t stream) {
+                           int ab, float alpha, float beta, int trans_a, int trans_b,
+                           cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(ceil_div(N, 64)), static_cast<unsigned>(ceil_div(M, 64)));
     const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
     switch (dtype) {
         case 0:
             generic_gemm_kernel<__half><<<grid, 256, 0, stream>>>(
                 static_cast<const __half*>(A), static_cast<const __half*>(B), C, m, n, k, lda, ldb, ldc,
-                ab, alpha, beta);
+                ab, alpha, beta, trans_a, trans_b);
             break;
         case 1:
             generic_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
                 static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), C, m, n,
-                k, lda, ldb, ldc, ab, alpha, beta);
+                k, lda, ldb, ldc, ab, alpha, beta, trans_a, trans_b);
             break;
         default:
             generic_gemm_kernel<float><<<grid, 256, 0, stream>>>(
                 static_cast<const float*>(A), static_cast<const float*>(B), C, m, n, k, lda, ldb, ldc,
-                ab, alpha, beta);
+                ab, alpha, beta, trans_a, trans_b);
             break;
     }
     return cudaGetLastError();

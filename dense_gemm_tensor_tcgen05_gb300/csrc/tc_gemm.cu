@@ -77,6 +77,8 @@ struct TcArgs {
     int32_t tma_store;          // epilogue writes C through the TMA store map
     int32_t ab;                 // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
     float alpha, beta;
+    int32_t p_kmajor;           // MMA A operand stored K-contiguous (else M/N-contiguous)
+    int32_t q_kmajor;           // MMA B operand stored K-contiguous (else M/N-contiguous)
     uint32_t idesc;
     float* ws;
     uint32_t* counters;
@@ -303,6 +305,44 @@ __device__ __forceinline__ void apply_ab(const TcArgs& a, float (&v)[W], int p, 
     }
 }
 
+// ---- operand layouts ----------------------------------------------------------
+//
+// Each MMA operand slice of R rows x 64 k sits in shared memory as R rows of
+// 128 bytes either way:
+//   K-major (K contiguous in memory): one TMA box {64 k, R rows} of a map
+//     whose inner dimension is K;
+//   MN-major (rows contiguous in memory): R/64 boxes {64 rows, 64 k} of a
+//     map whose inner dimension is the row dimension, 8 KiB apart.
+template <int R>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             bool kmajor, int r0, int k0) {
+    if (kmajor) {
+        tma_load_2d(dst, map, bar, k0, r0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < R / 64; ++j) tma_load_2d(dst + j * 8192, map, bar, r0 + 64 * j, k0);
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
+                                                  uint32_t bar, bool kmajor, int r0, int k0) {
+    if (kmajor) {
+        tma_load_2d_pair(dst, map, bar, k0, r0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < R / 64; ++j) tma_load_2d_pair(dst + j * 8192, map, bar, r0 + 64 * j, k0);
+    }
+}
+
+// Descriptor of k-step kk (16 k) of an operand slice: K-major steps 32 bytes
+// along each 128-byte row; MN-major steps 16 rows of 128 bytes and finds the
+// next 64-row block 8 KiB further (LBO).
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool kmajor, int kk) {
+    return kmajor ? smem_desc_sw128(base + kk * 32, 16, 1024)
+                  : smem_desc_sw128(base + kk * 2048, 8192, 1024);
+}
+
 // ---- TMA-store epilogue ------------------------------------------------------
 //
 // A warp's 32 accumulator rows x 32 columns (one chunk) go through a 4 KiB
@@ -423,16 +463,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     const uint32_t sp = smem_base + stage * T::kStageBytes;
                     const uint32_t sq = sp + T::kPBytes;
                     const int k0 = kb * kTcBK;
-                    if (!SWAP) {
-                        tma_load_2d(sp, &map_p, fb, k0, p0);                 // A: box {64 k, 128 rows}
-#pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)                    // B: boxes {64 cols, 64 k}
-                            tma_load_2d(sq + j * 8192, &map_q, fb, q0 + 64 * j, k0);
-                    } else {
-                        tma_load_2d(sp, &map_p, fb, p0, k0);                 // B: boxes {64 cols, 64 k}
-                        tma_load_2d(sp + 8192, &map_p, fb, p0 + 64, k0);
-                        tma_load_2d(sq, &map_q, fb, k0, q0);                 // A: box {64 k, BN rows}
-                    }
+                    load_operand<kTcBM>(sp, &map_p, fb, args.p_kmajor, p0, k0);
+                    load_operand<BN>(sq, &map_q, fb, args.q_kmajor, q0, k0);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -469,13 +501,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     const uint32_t sq = sp + T::kPBytes;
 #pragma unroll
                     for (int kk = 0; kk < kTcBK / kUmmaK; ++kk) {
-                        // K-major operand: next 16 k are 32 bytes further along each
-                        // 128-byte row.  MN-major operand: next 16 k are 16 rows of
-                        // 128 bytes further.
-                        const uint64_t adesc = SWAP ? smem_desc_sw128(sp + kk * 2048, 8192, 1024)
-                                                    : smem_desc_sw128(sp + kk * 32, 16, 1024);
-                        const uint64_t bdesc = SWAP ? smem_desc_sw128(sq + kk * 32, 16, 1024)
-                                                    : smem_desc_sw128(sq + kk * 2048, 8192, 1024);
+                        const uint64_t adesc = operand_desc(sp, args.p_kmajor, kk);
+                        const uint64_t bdesc = operand_desc(sq, args.q_kmajor, kk);
                         tc_mma_f16(d_tmem, adesc, bdesc, args.idesc,
                                    (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
@@ -753,10 +780,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const uint32_t sa = smem_base + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
                     const int k0 = kb * kTcBK;
-                    tma_load_2d_pair(sa, &map_a, fb, k0, m0);            // A: box {64 k, 128 rows}
-#pragma unroll
-                    for (int j = 0; j < BN / 128; ++j)                   // B: boxes {64 cols, 64 k}
-                        tma_load_2d_pair(sb + j * 8192, &map_b, fb, n0 + 64 * j, k0);
+                    load_operand_pair<kTcBM>(sa, &map_a, fb, args.p_kmajor, m0, k0);
+                    load_operand_pair<BN / 2>(sb, &map_b, fb, args.q_kmajor, n0, k0);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -790,8 +815,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const uint32_t sb = sa + T::kABytes;
 #pragma unroll
                     for (int kk = 0; kk < kTcBK / kUmmaK; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, 8192, 1024);
+                        const uint64_t adesc = operand_desc(sa, args.p_kmajor, kk);
+                        const uint64_t bdesc = operand_desc(sb, args.q_kmajor, kk);
                         tc_mma_f16_pair(d_tmem, adesc, bdesc, args.idesc,
                                         (kb > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -1023,13 +1048,21 @@ static cudaError_t launch_pair(const TcLaunch& L, const CUtensorMap& ma, const C
 cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t stream) {
     if (!tc_config_supported(L.bn, L.swap, L.pair)) return cudaErrorInvalidValue;
     if (L.pair && (L.splits != 1 || (L.grid & 1))) return cudaErrorInvalidValue;
-    // A: {K, M} (K contiguous); B: {N, K} (N contiguous).
-    CUtensorMap map_a, map_b;
+    // Operand roles: the MMA's A operand (128 rows) is op(A) -- or op(B)^T with
+    // swap -- and its B operand (BN rows; BN/2 per CTA in pairs) the other.
+    // A stored plain (M x K, trans_a = 0) is K-major; stored transposed
+    // (K x M) it is M-major.  B stored plain (K x N) is N-major; stored
+    // transposed (N x K) it is K-major.
+    const bool a_kmajor = !L.trans_a, b_kmajor = L.trans_b != 0;
     const uint32_t a_rows = L.swap ? static_cast<uint32_t>(L.bn) : kTcBM;
-    if (!encode_map(encode, &map_a, L.fmt, L.A, L.K, L.M, L.lda, 64, a_rows))
-        return cudaErrorInvalidValue;
-    if (!encode_map(encode, &map_b, L.fmt, L.B, L.N, L.K, L.ldb, 64, 64))
-        return cudaErrorInvalidValue;
+    const uint32_t b_rows = L.swap ? kTcBM : static_cast<uint32_t>(L.pair ? L.bn / 2 : L.bn);
+    if ((!a_kmajor && a_rows % 64) || (!b_kmajor && b_rows % 64)) return cudaErrorInvalidValue;
+    CUtensorMap map_a, map_b;
+    const bool ok_a = a_kmajor ? encode_map(encode, &map_a, L.fmt, L.A, L.K, L.M, L.lda, 64, a_rows)
+                               : encode_map(encode, &map_a, L.fmt, L.A, L.M, L.K, L.lda, 64, 64);
+    const bool ok_b = b_kmajor ? encode_map(encode, &map_b, L.fmt, L.B, L.K, L.N, L.ldb, 64, b_rows)
+                               : encode_map(encode, &map_b, L.fmt, L.B, L.N, L.K, L.ldb, 64, 64);
+    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
 
     TcArgs a;
     a.C = L.C;
@@ -1070,7 +1103,9 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
             a.tma_store = (L.store_mode == 1) ? 0 : 1;
     }
-    a.idesc = idesc_f16_f32(static_cast<uint32_t>(L.fmt), L.swap != 0, L.swap == 0,
+    a.p_kmajor = L.swap ? b_kmajor : a_kmajor;
+    a.q_kmajor = L.swap ? a_kmajor : b_kmajor;
+    a.idesc = idesc_f16_f32(static_cast<uint32_t>(L.fmt), !a.p_kmajor, !a.q_kmajor,
                             L.pair ? 2 * kTcBM : kTcBM, static_cast<uint32_t>(L.bn));
     a.ws = L.ws;
     a.counters = L.counters;

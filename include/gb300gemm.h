@@ -126,7 +126,16 @@ gemm_status_t sgemm_f32(const float *A, const float *B, float *C,
  *             operation ("04-wmma-matmul", header comment: D = A*B + C).  The
  *             product is accumulated in FP32, then scaled and added in FP32.
  *             With beta == 0, C is not read (it may hold anything, NaN
- *             included).  With K == 0 the result is beta * C.  Stream-K keeps
+ *             included).  With K == 0 the result is beta * C.
+ *   trans_a   0 = A is op(A), stored M x K (lda >= K); 1 = A is stored as its
+ *             transpose, K x M row-major (lda >= M), and the product uses Aᵀ.
+ *   trans_b   0 = B stored K x N (ldb >= N); 1 = B stored as its transpose,
+ *             N x K (ldb >= K).  Together: C = op(A) x op(B), the row-major
+ *             reading of the transposition the pages use to call a
+ *             column-major library ("matmul_registers.cu", the cuBLAS call).
+ *             The tensor-core kernels read either layout directly (TMA boxes
+ *             and MMA descriptors per layout); FP32 with a transpose runs the
+ *             guarded CUDA-core kernel.  gemm_ex_host takes no transposes.  Stream-K keeps
  *             whole tiles while whole waves last and shares the remaining
  *             tiles' k-blocks evenly over all CTAs; a tile cut into pieces
  *             is summed in a fixed order.  Ignored with split_k > 0.
@@ -145,6 +154,9 @@ typedef struct {
     float alpha;
     float beta;
     int32_t epilogue;
+    int32_t trans_a;
+    int32_t trans_b;
+    int32_t reserved[2];
 } gemm_options_t;
 
 /* gemm_ex -- the same operation with an explicit plan (tests and tuning). */

@@ -95,3 +95,15 @@ def test_python_binding_raises_gemm_error(L):
     with pytest.raises(g.GemmError) as e:
         g.gemm_f16f32(P, 2 * P, 3 * P, -1, 4, 4, 4, 4, 4)
     assert e.value.status == 1 and e.value.name == "GEMM_ERR_INVALID_VALUE"
+
+
+def test_transposed_leading_dimensions_checked_on_host(L):
+    o = g.GemmOptions()
+    o.dtype, o.swap_ab, o.trans_a = 0, -1, 1
+    # trans_a: A is K x M, so lda must be >= M = 8
+    assert L.gemm_ex(P, 2 * P, 3 * P, 8, 4, 4, 4, 4, 4, ctypes.byref(o), None) == 1
+    o.trans_a, o.trans_b = 0, 1
+    # trans_b: B is N x K, so ldb must be >= K = 6
+    assert L.gemm_ex(P, 2 * P, 3 * P, 4, 4, 6, 6, 4, 4, ctypes.byref(o), None) == 1
+    o.trans_b = 2
+    assert L.gemm_ex(P, 2 * P, 3 * P, 4, 4, 4, 4, 4, 4, ctypes.byref(o), None) == 1
