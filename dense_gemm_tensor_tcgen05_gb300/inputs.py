@@ -49,7 +49,7 @@ _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-DTYPES = ("f16", "bf16", "f32")
+DTYPES = ("f16", "bf16", "f32", "e4m3", "e5m2")
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -111,14 +111,25 @@ def round_to_f16_bits(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
 
 
+def round_to_fp8_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """FP32 -> E4M3 / E5M2 bits (torch's round-to-nearest-even conversion;
+    inputs are expected within range: |x| <= 448 for E4M3)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    tt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+    return t.to(tt).view(torch.uint8).numpy().copy()
+
+
 def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     """Round FP32 values to ``dtype`` and return the element bits
-    (uint16 for f16/bf16; float32 itself for f32)."""
+    (uint8 for e4m3/e5m2; uint16 for f16/bf16; float32 itself for f32)."""
     if dtype == "f16":
         return round_to_f16_bits(x)
     if dtype == "bf16":
         return round_to_bf16_bits(x)
-    if dtype == "f32":
+    if dtype in ("e4m3", "e5m2"):
+        return round_to_fp8_bits(x, dtype)
+    if dtype in ("f32", "tf32"):
         return np.ascontiguousarray(x, dtype=np.float32)
     raise ValueError(f"unknown dtype {dtype!r}")
 
@@ -133,6 +144,11 @@ def bits_abs_max(bits: np.ndarray, dtype: str) -> float:
     if dtype == "bf16":
         v = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
         return float(np.abs(v).max())
+    if dtype in ("e4m3", "e5m2"):
+        import torch
+        tt = torch.float8_e4m3fn if dtype == "e4m3" else torch.float8_e5m2
+        v = torch.from_numpy(np.ascontiguousarray(bits)).view(tt).float()
+        return float(v.abs().max())
     return float(np.abs(bits.astype(np.float32)).max())
 
 
@@ -146,6 +162,8 @@ def padded(x: np.ndarray, ld: int) -> np.ndarray:
     out = np.empty((rows, ld), dtype=x.dtype)
     if x.dtype == np.float32:
         out[...] = np.float32(1e30)
+    elif x.dtype == np.uint8:
+        out[...] = 0x7E     # 448 (E4M3) / 5.7e4 (E5M2): large and finite
     else:
         out[...] = 0x7BFF   # large finite in FP16; ~1.1e36 in BF16
     out[:, :cols] = x

@@ -42,14 +42,15 @@ import numpy as np
 
 __all__ = [
     "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows", "gemm_general", "gemm_op",
-    "general_bounds",
+    "general_bounds", "tf32_bound", "E4M3", "E5M2",
     "gemm_entries", "compare", "Comparison", "ABS_COEF", "REL_FROB",
 ]
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 _DTYPE_NAMES = {"f16": F16, "fp16": F16, "float16": F16,
                 "bf16": BF16, "bfloat16": BF16,
-                "f32": F32, "fp32": F32, "float32": F32}
+                "f32": F32, "fp32": F32, "float32": F32, "tf32": F32,
+                "e4m3": E4M3, "e5m2": E5M2}
 
 ABS_COEF = 1e-3
 REL_FROB = 1e-4
@@ -95,6 +96,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_bf16_to_f64.restype = ctypes.c_double
             L.oracle_f32_to_f64.argtypes = [ctypes.c_uint32]
             L.oracle_f32_to_f64.restype = ctypes.c_double
+            L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_to_f64.restype = ctypes.c_double
+            L.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
+            L.oracle_e5m2_to_f64.restype = ctypes.c_double
             L.oracle_decode.argtypes = [ctypes.c_int, vp, dp, i64]
             L.oracle_decode.restype = ctypes.c_int
             L.oracle_gemm_rows.argtypes = [ctypes.c_int, vp, vp, dp, i64, i64, i64,
@@ -120,7 +125,7 @@ def lib() -> ctypes.CDLL:
 
 def _dtype_code(dtype) -> int:
     if isinstance(dtype, int):
-        if dtype not in (F16, BF16, F32):
+        if dtype not in (F16, BF16, F32, E4M3, E5M2):
             raise ValueError(f"bad dtype code {dtype}")
         return dtype
     try:
@@ -130,10 +135,11 @@ def _dtype_code(dtype) -> int:
 
 
 def _bits(x: np.ndarray, code: int) -> np.ndarray:
-    """Raw element bits as a C-contiguous array (uint16 for 16-bit types,
-    uint32 for FP32).  FP32 may be given as float32 and is reinterpreted."""
+    """Raw element bits as a C-contiguous array (uint8 for 8-bit types,
+    uint16 for 16-bit types, uint32 for FP32).  FP32 may be given as float32
+    and is reinterpreted."""
     x = np.asarray(x)
-    want = np.uint16 if code in (F16, BF16) else np.uint32
+    want = np.uint8 if code in (E4M3, E5M2) else np.uint16 if code in (F16, BF16) else np.uint32
     if x.dtype.itemsize != np.dtype(want).itemsize:
         raise TypeError(f"expected {np.dtype(want).itemsize}-byte elements, got {x.dtype}")
     return np.ascontiguousarray(x).view(want)
@@ -229,6 +235,16 @@ def gemm_op(dtype, trans_a: bool, trans_b: bool, A, B, M: int, N: int, K: int,
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_op failed ({rc})")
     return C
+
+
+def tf32_bound(abs_sums: np.ndarray) -> np.ndarray:
+    """Per-element tolerance for TF32 tensor-core products of FP32 inputs:
+    TF32 keeps 10 fraction bits, so each input carries a relative error below
+    2^-10 and each product below 2^-9 (whether the hardware rounds or drops
+    the low 13 bits); FP32 accumulation adds about 2^-20 of the sum of
+    magnitudes.  abs_sums[i, j] = sum_k |A[i][k]| |B[k][j]| (the oracle's
+    product of the absolute values)."""
+    return (2.0 ** -9 + 2.0 ** -20) * np.asarray(abs_sums, dtype=np.float64)
 
 
 def general_bounds(K: int, max_abs_a: float, max_abs_b: float, alpha: float, beta: float,

@@ -41,7 +41,7 @@
 
 /* dtype codes shared with the Python wrapper of this oracle (not with the
  * CUDA library). */
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
 
 /* ---- scalar decoders ---------------------------------------------------- */
 
@@ -102,19 +102,58 @@ double oracle_f32_to_f64(uint32_t w)
     return s ? -v : v;
 }
 
+/* 8-bit floating point, E4M3: 1 sign bit, 4 exponent bits (bias 7), 3
+ * fraction bits; no infinities, and exponent 15 with fraction 7 is NaN.
+ * exponent 0 -> (-1)^s * 2^-6 * (f / 8); otherwise (-1)^s * 2^(e-7) * (1 + f/8). */
+double oracle_e4m3_to_f64(uint8_t x)
+{
+    int s = (x >> 7) & 1;
+    int e = (x >> 3) & 0xf;
+    int f = x & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);                /* 2^-6 * f / 2^3 */
+    else
+        v = ldexp((double)(8 + f), e - 10);      /* 2^(e-7) * (8+f)/2^3 */
+    return s ? -v : v;
+}
+
+/* 8-bit floating point, E5M2: 1 sign bit, 5 exponent bits (bias 15), 2
+ * fraction bits, with IEEE-style infinities and NaNs at exponent 31. */
+double oracle_e5m2_to_f64(uint8_t x)
+{
+    int s = (x >> 7) & 1;
+    int e = (x >> 2) & 0x1f;
+    int f = x & 0x3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -16);               /* 2^-14 * f / 2^2 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(4 + f), e - 17);      /* 2^(e-15) * (4+f)/2^2 */
+    return s ? -v : v;
+}
+
 static double decode_one(int dtype, const void *base, int64_t idx)
 {
     if (dtype == ORACLE_F16)
         return oracle_f16_to_f64(((const uint16_t *)base)[idx]);
     if (dtype == ORACLE_BF16)
         return oracle_bf16_to_f64(((const uint16_t *)base)[idx]);
+    if (dtype == ORACLE_E4M3)
+        return oracle_e4m3_to_f64(((const uint8_t *)base)[idx]);
+    if (dtype == ORACLE_E5M2)
+        return oracle_e5m2_to_f64(((const uint8_t *)base)[idx]);
     return oracle_f32_to_f64(((const uint32_t *)base)[idx]);
 }
 
 /* Decode n elements to double. Returns 0, or -1 on a bad dtype. */
 int oracle_decode(int dtype, const void *src, double *dst, int64_t n)
 {
-    if (dtype < ORACLE_F16 || dtype > ORACLE_F32)
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2)
         return -1;
     for (int64_t i = 0; i < n; ++i)
         dst[i] = decode_one(dtype, src, i);
@@ -162,7 +201,7 @@ int oracle_gemm_rows(int dtype, const void *A, const void *B, double *C,
                      int64_t lda, int64_t ldb, int64_t ldc,
                      int64_t row0, int64_t row1, int nthreads)
 {
-    if (dtype < ORACLE_F16 || dtype > ORACLE_F32)
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2)
         return -1;
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N)
         return -1;
@@ -251,7 +290,7 @@ int oracle_gemm_entries(int dtype, const void *A, const void *B,
                         int64_t count, const int64_t *rows, const int64_t *cols,
                         double *out)
 {
-    if (dtype < ORACLE_F16 || dtype > ORACLE_F32)
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2)
         return -1;
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || count < 0)
         return -1;
@@ -317,7 +356,7 @@ int oracle_gemm_op(int dtype, int trans_a, int trans_b, const void *A, const voi
                    double *C, int64_t M, int64_t N, int64_t K,
                    int64_t lda, int64_t ldb, int64_t ldc, int nthreads)
 {
-    if (dtype < ORACLE_F16 || dtype > ORACLE_F32)
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E5M2)
         return -1;
     if (M < 0 || N < 0 || K < 0 || ldc < N)
         return -1;
