@@ -23,8 +23,8 @@ import threading
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
     "gemm_ex_noalloc", "gemm_ex_host", "gemm_plan_describe", "gemm_device_error",
-    "gemm_watchdog_selftest", "gemm_release_workspace", "gemm_version",
-    "gemm_launch_count", "matmul", "plan", "GemmOptions", "STATUS", "EXPORTED_SYMBOLS",
+    "gemm_watchdog_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt", "gemm_e5m2f32_bt",
+    "gemm_release_workspace", "gemm_version", "gemm_launch_count", "matmul", "plan", "GemmOptions", "STATUS", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -46,7 +46,8 @@ EXPORTED_SYMBOLS = (
     "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex", "gemm_plan_describe",
     "gemm_device_error", "gemm_release_workspace", "gemm_status_string",
     "gemm_last_cuda_error", "gemm_version", "gemm_launch_count", "gemm_ex_noalloc",
-    "gemm_ex_host", "gemm_watchdog_selftest",
+    "gemm_ex_host", "gemm_watchdog_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt",
+    "gemm_e5m2f32_bt",
 )
 
 
@@ -87,7 +88,8 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(library_path)
             vp, i64 = ctypes.c_void_p, ctypes.c_int64
             sig = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
-            for name in ("gemm_f16f32", "gemm_bf16f32", "sgemm_f32"):
+            for name in ("gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_tf32f32_bt",
+                         "gemm_e4m3f32_bt", "gemm_e5m2f32_bt"):
                 f = getattr(L, name)
                 f.argtypes = sig
                 f.restype = ctypes.c_int
@@ -142,6 +144,21 @@ def gemm_bf16f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: 
 def sgemm_f32(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
               stream: int = 0) -> None:
     _check(lib().sgemm_f32(A, B, C, M, N, K, lda, ldb, ldc, stream or None))
+
+
+def gemm_tf32f32_bt(A: int, Bt: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                    ldc: int, stream: int = 0) -> None:
+    _check(lib().gemm_tf32f32_bt(A, Bt, C, M, N, K, lda, ldb, ldc, stream or None))
+
+
+def gemm_e4m3f32_bt(A: int, Bt: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                    ldc: int, stream: int = 0) -> None:
+    _check(lib().gemm_e4m3f32_bt(A, Bt, C, M, N, K, lda, ldb, ldc, stream or None))
+
+
+def gemm_e5m2f32_bt(A: int, Bt: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                    ldc: int, stream: int = 0) -> None:
+    _check(lib().gemm_e5m2f32_bt(A, Bt, C, M, N, K, lda, ldb, ldc, stream or None))
 
 
 def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0,
@@ -214,7 +231,8 @@ def gemm_launch_count() -> int:
 
 # ---- torch convenience -------------------------------------------------------
 
-_DTYPE_CODE = {"float16": 0, "bfloat16": 1, "float32": 2}
+_DTYPE_CODE = {"float16": 0, "bfloat16": 1, "float32": 2, "float8_e4m3fn": 4,
+               "float8_e5m2": 5}
 
 
 def _code(t) -> int:
@@ -246,10 +264,13 @@ def _operand_layout(t, name: str):
     raise ValueError(f"{name} must be row-major or column-major")
 
 
-def matmul(A, B, out=None, stream=None, **opts):
+def matmul(A, B, out=None, stream=None, tf32=False, **opts):
     """C = A @ B for 2-D tensors (row-major, any row stride).
 
-    A and B: both float16, both bfloat16 or both float32; C is float32.
+    A and B: both float16, both bfloat16, both float32, both float8_e4m3fn
+    or both float8_e5m2; C is float32.  ``tf32=True`` runs float32 inputs on
+    the tensor cores as TF32.  FP8 and TF32 products need A row-major and B
+    column-major (B = Bt.t() for a row-major N x K Bt), on the GPU.
     CUDA tensors run gemm_f16f32 / gemm_bf16f32 / sgemm_f32 (or gemm_ex when
     plan options are given) on the current (or given) stream and return at
     once.  CPU tensors go through gemm_ex_host -- the library copies them in,
@@ -265,6 +286,10 @@ def matmul(A, B, out=None, stream=None, **opts):
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
     code = _code(A)
+    if tf32:
+        if code != 2:
+            raise TypeError("tf32=True needs float32 operands")
+        code = 3
     if A.is_cuda != B.is_cuda:
         raise ValueError("A and B must both be on the GPU or both on the host")
     M, K = A.shape
@@ -290,6 +315,8 @@ def matmul(A, B, out=None, stream=None, **opts):
     ldc = _row_major_ld(out, "C")
     ta, lda = _operand_layout(A, "A")
     tb, ldb = _operand_layout(B, "B")
+    if code >= 3 and (ta, tb) != (0, 1):
+        raise ValueError("TF32 and FP8 products need A row-major and B column-major")
     if ta or tb:
         opts = dict(opts, trans_a=ta, trans_b=tb)
     args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc)
@@ -305,13 +332,19 @@ def matmul(A, B, out=None, stream=None, **opts):
     return out
 
 
-def plan(A, B, out=None, **opts) -> str:
+def plan(A, B, out=None, tf32=False, **opts) -> str:
     """The plan text gemm_plan_describe gives for torch tensors A @ B."""
     code = _code(A)
+    if tf32 and code == 2:
+        code = 3
     M, K = A.shape
     _, N = B.shape
     # Only C's alignment is read; without `out`, describe a 256-byte aligned C.
     cptr = out.data_ptr() if out is not None else 256
     ldc = _row_major_ld(out, "C") if out is not None else N
+    ta, lda = _operand_layout(A, "A")
+    tb, ldb = _operand_layout(B, "B")
+    if ta or tb:
+        opts = dict(opts, trans_a=ta, trans_b=tb)
     return gemm_plan_describe(code, A.data_ptr(), B.data_ptr(), cptr, M, N, K,
-                              _row_major_ld(A, "A"), _row_major_ld(B, "B"), ldc, **opts)
+                              lda, ldb, ldc, **opts)

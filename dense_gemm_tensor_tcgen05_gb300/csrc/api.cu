@@ -176,6 +176,11 @@ gemm_status_t get_workspace(int dev, cudaStream_t stream, size_t floats, size_t 
 
 // ---- argument checks -------------------------------------------------------------
 
+// dtype codes of gemm_options_t: 0 FP16, 1 BF16, 2 FP32 (CUDA cores), 3 TF32
+// (FP32 storage, tensor cores), 4 E4M3, 5 E5M2.
+int dtype_bytes(int dtype) { return dtype <= 1 ? 2 : dtype <= 3 ? 4 : 1; }
+int tc_fmt_of(int dtype) { return dtype <= 1 ? dtype : dtype - 1; }
+
 bool spans_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
     return a0 < b1 && b0 < a1;
 }
@@ -321,10 +326,15 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
         return GEMM_OK;
     }
 
-    // 16-bit inputs: TMA needs 16-byte aligned bases and row strides.
+    // Tensor-core inputs: TMA needs 16-byte aligned bases and row strides.
+    const int es = dtype_bytes(dtype);
     const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0 &&
-                        (lda & 7) == 0 && (ldb & 7) == 0;
-    if (o.generic || !tma_ok) {
+                        (lda * es) % 16 == 0 && (ldb * es) % 16 == 0;
+    if (dtype >= 3) {
+        // TF32 and 8-bit inputs run only on the tensor cores, with both
+        // operands K-contiguous: A stored M x K, B stored N x K.
+        if (o.generic || !tma_ok || o.trans_a || !o.trans_b) return GEMM_ERR_INVALID_VALUE;
+    } else if (o.generic || !tma_ok) {
         p.kind = Kind::Generic;
         *plan = p;
         return GEMM_OK;
@@ -337,7 +347,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     L.beta = p.beta;
     L.A = A; L.B = B; L.C = C;
     L.M = M; L.N = N; L.K = K; L.lda = lda; L.ldb = ldb; L.ldc = ldc;
-    L.fmt = dtype;
+    L.fmt = tc_fmt_of(dtype);
     L.swap = (o.swap_ab < 0) ? ((M <= 64 && N > M) ? 1 : 0) : (o.swap_ab ? 1 : 0);
     if (o.cta_pair < 0 || o.cta_pair > 2) return GEMM_ERR_INVALID_VALUE;
     if (o.store_mode < 0 || o.store_mode > 1) return GEMM_ERR_INVALID_VALUE;
@@ -399,7 +409,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     }
     const int64_t tiles_p = ceil_div(pe, kTcBM);
     const int64_t tiles = tiles_p * ceil_div(qe, L.bn);
-    const int64_t kb_total = ceil_div(K, kTcBK);
+    const int64_t kb_total = ceil_div(K, tc_k_elems(L.fmt));
 
     if (o.stream_k < 0 || o.stream_k > 2) return GEMM_ERR_INVALID_VALUE;
     int64_t group = o.group_m > 0 ? o.group_m : 16;
@@ -460,6 +470,11 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
 
 void describe_kernel(const Plan& p, int dtype, char* buf, int n);
 
+const char* fmt_name(int fmt) {
+    static const char* names[] = {"f16", "bf16", "tf32", "e4m3", "e5m2"};
+    return (fmt >= 0 && fmt <= 4) ? names[fmt] : "?";
+}
+
 void describe(const Plan& p, int dtype, char* buf, int64_t size) {
     if (!buf || size <= 0) return;
     const int n = static_cast<int>(size > INT32_MAX ? INT32_MAX : size);
@@ -493,13 +508,13 @@ void describe_kernel(const Plan& p, int dtype, char* buf, int n) {
                 snprintf(buf, n,
                          "tcgen05 fmt=%s tile=%dx%d pair=%d swap=%d stream_k dp_tiles=%d sk_kblocks=%lld "
                          "max_seg=%d group=%d units=%lld grid=%d",
-                         p.tc.fmt ? "bf16" : "f16", p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
+                         fmt_name(p.tc.fmt), p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
                          p.tc.swap, p.tc.dp_tiles, static_cast<long long>(p.tc.sk_kblocks),
                          p.tc.max_seg, p.tc.group, static_cast<long long>(p.units), p.tc.grid);
             else
                 snprintf(buf, n,
                          "tcgen05 fmt=%s tile=%dx%d pair=%d swap=%d split_k=%d group=%d units=%lld grid=%d",
-                         p.tc.fmt ? "bf16" : "f16", p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
+                         fmt_name(p.tc.fmt), p.tc.pair ? 256 : 128, p.tc.bn, p.tc.pair,
                          p.tc.swap, p.tc.splits, p.tc.group, static_cast<long long>(p.units), p.tc.grid);
             break;
     }
@@ -518,8 +533,8 @@ gemm_status_t launch_status(cudaError_t e, const char* what) {
 gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, int64_t N,
                   int64_t K, int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t& o,
                   cudaStream_t stream) {
-    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
-    const int esize = dtype == 2 ? 4 : 2;
+    if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
+    const int esize = dtype_bytes(dtype);
     gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize, o.trans_a, o.trans_b);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -592,6 +607,32 @@ gemm_status_t sgemm_f32(const float* A, const float* B, float* C, int64_t M, int
                reinterpret_cast<cudaStream_t>(stream));
 }
 
+static gemm_status_t run_bt(int dtype, const void* A, const void* Bt, float* C, int64_t M,
+                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                            gemm_stream_t stream) {
+    gemm_options_t o = default_options(dtype);
+    o.trans_b = 1;
+    return run(dtype, A, Bt, C, M, N, K, lda, ldb, ldc, o, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_tf32f32_bt(const float* A, const float* Bt, float* C, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream) {
+    return run_bt(3, A, Bt, C, M, N, K, lda, ldb, ldc, stream);
+}
+
+gemm_status_t gemm_e4m3f32_bt(const void* A, const void* Bt, float* C, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream) {
+    return run_bt(4, A, Bt, C, M, N, K, lda, ldb, ldc, stream);
+}
+
+gemm_status_t gemm_e5m2f32_bt(const void* A, const void* Bt, float* C, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream) {
+    return run_bt(5, A, Bt, C, M, N, K, lda, ldb, ldc, stream);
+}
+
 gemm_status_t gemm_ex(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t* options,
                       gemm_stream_t stream) {
@@ -605,9 +646,9 @@ gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, co
                                  int64_t ldc, const gemm_options_t* options, char* buf,
                                  int64_t size) {
     if (buf && size > 0) buf[0] = '\0';
-    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
+    if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     gemm_options_t o = options ? *options : default_options(dtype);
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2, o.trans_a,
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype_bytes(dtype), o.trans_a,
                                   o.trans_b);
     if (st != GEMM_OK) return st;
     int dev;
@@ -806,8 +847,8 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
                                          gemm_stream_t stream_handle) {
     if (!options) return GEMM_ERR_INVALID_VALUE;
     const int dtype = options->dtype;
-    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype == 2 ? 4 : 2,
+    if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype_bytes(dtype),
                                   options->trans_a, options->trans_b);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -951,8 +992,8 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
                                       const gemm_options_t* options, gemm_stream_t stream_handle) {
     if (!options) return GEMM_ERR_INVALID_VALUE;
     const int dtype = options->dtype;
-    if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_VALUE;
-    const size_t es = dtype == 2 ? 4 : 2;
+    if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
+    const size_t es = dtype_bytes(dtype);
     if (options->trans_a || options->trans_b) return GEMM_ERR_INVALID_VALUE;
     gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es));
     if (st != GEMM_OK) return st;

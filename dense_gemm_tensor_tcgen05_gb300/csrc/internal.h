@@ -19,7 +19,7 @@ struct TcLaunch {
     const void* B;
     float* C;
     int64_t M, N, K, lda, ldb, ldc;
-    int fmt;        // 0 = FP16, 1 = BF16
+    int fmt;        // 0 = FP16, 1 = BF16, 2 = TF32 (FP32 storage), 3 = E4M3, 4 = E5M2
     int bn;         // tile width along the MMA N side
     int swap;       // 1: MMA M side runs along N of C (C^T = B^T A^T)
     int pair;       // 1: CTA-pair kernel (clusters of 2, 256 x bn tiles)
@@ -48,6 +48,12 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // k-blocks on at most `sms` CTAs: fills dp_tiles, sk_kblocks, max_seg, grid
 // of L and returns the number of tiles that need workspace slots.
 int64_t tc_streamk_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sms);
+
+// MMA kind of an input format (0: 16-bit, 1: TF32, 2: 8-bit), its element
+// size in bytes, and the K elements one 128-byte stage row holds.
+int tc_kind(int fmt);
+int tc_elem_bytes(int fmt);
+inline int tc_k_elems(int fmt) { return 128 / tc_elem_bytes(fmt); }
 
 // Which (bn, swap, pair) kernels exist.
 bool tc_config_supported(int bn, int swap, int pair);

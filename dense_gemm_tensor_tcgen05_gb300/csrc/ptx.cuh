@@ -144,6 +144,31 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// MMA kinds: 0 = kind::f16 (FP16 / BF16 inputs, K = 16 per instruction),
+// 1 = kind::tf32 (FP32 storage read as TF32, K = 8), 2 = kind::f8f6f4 (here
+// E4M3 / E5M2, K = 32).  Each instruction consumes 32 bytes of K per row.
+template <int KIND>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    if constexpr (KIND == 0) {
+        tc_mma_f16(d_tmem, a_desc, b_desc, idesc, accumulate);
+    } else if constexpr (KIND == 1) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued
 // before it has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -290,6 +315,28 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+template <int KIND>
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    if constexpr (KIND == 0) {
+        tc_mma_f16_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
+    } else if constexpr (KIND == 1) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
+}
+
 // Arrive once on the mbarrier at this shared-memory offset in every CTA of
 // `cta_mask` when all pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {
@@ -326,9 +373,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor for kind::f16 with an FP32 accumulator.
-//   bits 4-5 D format (1 = F32); 7-9 A format, 10-12 B format (0 = F16,
-//   1 = BF16); bit 15 A is MN-major; bit 16 B is MN-major; bits 17-22 N >> 3;
+// Instruction descriptor with an FP32 accumulator (same layout for
+// kind::f16, kind::tf32 and kind::f8f6f4).
+//   bits 4-5 D format (1 = F32); 7-9 A format, 10-12 B format (kind::f16:
+//   0 = F16, 1 = BF16; kind::tf32: 2 = TF32; kind::f8f6f4: 0 = E4M3,
+//   1 = E5M2); bit 15 A is MN-major; bit 16 B is MN-major; bits 17-22 N >> 3;
 //   bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t ab_format, bool a_mn_major,
                                                      bool b_mn_major, uint32_t m, uint32_t n) {

@@ -59,6 +59,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitim
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s for copies already in flight
 constexpr int kThreads = 192;
 constexpr int kUmmaK = 16;
+constexpr int kMmasPerStage = 4;   // each MMA takes 32 of a stage's 128 bytes of K per row
+
+// Elements of K per 128-byte stage row for an MMA kind (0: 16-bit, 1: TF32,
+// 2: 8-bit).
+__host__ __device__ constexpr int kind_k_elems(int kind) {
+    return kind == 0 ? 64 : kind == 1 ? 32 : 128;
+}
 constexpr int kStoreStageBytes = 4 * 2 * 4096;   // epilogue staging: 4 warps x two 4 KiB buffers
 
 struct TcArgs {
@@ -384,7 +391,7 @@ __device__ __forceinline__ void stage_and_store(StoreStage& st, const CUtensorMa
 
 // ---- the kernel ---------------------------------------------------------------
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_q,
                const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
@@ -462,7 +469,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t sp = smem_base + stage * T::kStageBytes;
                     const uint32_t sq = sp + T::kPBytes;
-                    const int k0 = kb * kTcBK;
+                    const int k0 = kb * kind_k_elems(KIND);
                     load_operand<kTcBM>(sp, &map_p, fb, args.p_kmajor, p0, k0);
                     load_operand<BN>(sq, &map_q, fb, args.q_kmajor, q0, k0);
                     if (++stage == S) {
@@ -500,10 +507,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     const uint32_t sp = smem_base + stage * T::kStageBytes;
                     const uint32_t sq = sp + T::kPBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kTcBK / kUmmaK; ++kk) {
+                    for (int kk = 0; kk < kMmasPerStage; ++kk) {
                         const uint64_t adesc = operand_desc(sp, args.p_kmajor, kk);
                         const uint64_t bdesc = operand_desc(sq, args.q_kmajor, kk);
-                        tc_mma_f16(d_tmem, adesc, bdesc, args.idesc,
+                        tc_mma<KIND>(d_tmem, adesc, bdesc, args.idesc,
                                    (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));   // stage is free once these MMAs finish
@@ -694,7 +701,7 @@ __device__ __forceinline__ bool pair_wait_phase(uint32_t bar, uint32_t parity,
     }
 }
 
-template <int BN>
+template <int BN, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ CUtensorMap map_c, const TcArgs args) {
@@ -779,7 +786,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     const uint32_t sa = smem_base + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
-                    const int k0 = kb * kTcBK;
+                    const int k0 = kb * kind_k_elems(KIND);
                     load_operand_pair<kTcBM>(sa, &map_a, fb, args.p_kmajor, m0, k0);
                     load_operand_pair<BN / 2>(sb, &map_b, fb, args.q_kmajor, n0, k0);
                     if (++stage == S) {
@@ -814,10 +821,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const uint32_t sa = smem_base + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kTcBK / kUmmaK; ++kk) {
+                    for (int kk = 0; kk < kMmasPerStage; ++kk) {
                         const uint64_t adesc = operand_desc(sa, args.p_kmajor, kk);
                         const uint64_t bdesc = operand_desc(sb, args.q_kmajor, kk);
-                        tc_mma_f16_pair(d_tmem, adesc, bdesc, args.idesc,
+                        tc_mma_pair<KIND>(d_tmem, adesc, bdesc, args.idesc,
                                         (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit_pair_multicast(empty_bar(stage), 0x3);
@@ -984,7 +991,7 @@ static cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchA
 
 template <int BN>
 static cudaError_t pair_max_clusters_for(int* n) {
-    auto kern = tc_gemm_pair_kernel<BN>;
+    auto kern = tc_gemm_pair_kernel<BN, 0>;   // residency is the same for every kind
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PairTraits<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1004,26 +1011,32 @@ cudaError_t tc_error_word(uint32_t** ptr) {
     return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_tc_error);
 }
 
+// fmt: 0 FP16, 1 BF16, 2 TF32 (FP32 storage), 3 E4M3, 4 E5M2.
+int tc_kind(int fmt) { return fmt <= 1 ? 0 : fmt == 2 ? 1 : 2; }
+int tc_elem_bytes(int fmt) { return fmt <= 1 ? 2 : fmt == 2 ? 4 : 1; }
+
 static bool encode_map(EncodeTiledFn encode, CUtensorMap* map, int fmt, const void* base,
                        uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box_inner,
                        uint32_t box_outer) {
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {ld_elems * 2};
+    const cuuint64_t strides[1] = {ld_elems * tc_elem_bytes(fmt)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
-        fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+        : fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+        : fmt == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     CUresult r = encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int KIND>
 static cudaError_t launch_cfg(const TcLaunch& L, const CUtensorMap& mp, const CUtensorMap& mq,
                               const CUtensorMap& mc, const TcArgs& args, cudaStream_t stream) {
     using T = TcTraits<BN, SWAP>;
-    auto kern = tc_gemm_kernel<BN, SWAP>;
+    auto kern = tc_gemm_kernel<BN, SWAP, KIND>;
     // The attribute is per device; setting it every call is cheap and keeps
     // multi-device use correct.
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1033,16 +1046,43 @@ static cudaError_t launch_cfg(const TcLaunch& L, const CUtensorMap& mp, const CU
     return cudaGetLastError();
 }
 
-template <int BN>
+template <int BN, int KIND>
 static cudaError_t launch_pair(const TcLaunch& L, const CUtensorMap& ma, const CUtensorMap& mb,
                                const CUtensorMap& mc, const TcArgs& args, cudaStream_t stream) {
-    auto kern = tc_gemm_pair_kernel<BN>;
+    auto kern = tc_gemm_pair_kernel<BN, KIND>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PairTraits<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pair_config<BN>(L.grid, stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, args);
+}
+
+template <int KIND>
+static cudaError_t dispatch_kind(const TcLaunch& L, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                 const CUtensorMap& mp, const CUtensorMap& mq, const CUtensorMap& map_c,
+                                 const TcArgs& a, cudaStream_t stream) {
+    if (L.pair) {
+        switch (L.bn) {
+            case 128: return launch_pair<128, KIND>(L, map_a, map_b, map_c, a, stream);
+            case 256: return launch_pair<256, KIND>(L, map_a, map_b, map_c, a, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
+    if (!L.swap) {
+        switch (L.bn) {
+            case 64: return launch_cfg<64, false, KIND>(L, mp, mq, map_c, a, stream);
+            case 128: return launch_cfg<128, false, KIND>(L, mp, mq, map_c, a, stream);
+            case 256: return launch_cfg<256, false, KIND>(L, mp, mq, map_c, a, stream);
+        }
+    } else {
+        switch (L.bn) {
+            case 16: return launch_cfg<16, true, KIND>(L, mp, mq, map_c, a, stream);
+            case 32: return launch_cfg<32, true, KIND>(L, mp, mq, map_c, a, stream);
+            case 64: return launch_cfg<64, true, KIND>(L, mp, mq, map_c, a, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t stream) {
@@ -1057,10 +1097,13 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     const uint32_t a_rows = L.swap ? static_cast<uint32_t>(L.bn) : kTcBM;
     const uint32_t b_rows = L.swap ? kTcBM : static_cast<uint32_t>(L.pair ? L.bn / 2 : L.bn);
     if ((!a_kmajor && a_rows % 64) || (!b_kmajor && b_rows % 64)) return cudaErrorInvalidValue;
+    // TF32 and 8-bit operands are read K-major only
+    if (tc_kind(L.fmt) != 0 && (!a_kmajor || !b_kmajor)) return cudaErrorInvalidValue;
+    const uint32_t ke = static_cast<uint32_t>(kind_k_elems(tc_kind(L.fmt)));
     CUtensorMap map_a, map_b;
-    const bool ok_a = a_kmajor ? encode_map(encode, &map_a, L.fmt, L.A, L.K, L.M, L.lda, 64, a_rows)
+    const bool ok_a = a_kmajor ? encode_map(encode, &map_a, L.fmt, L.A, L.K, L.M, L.lda, ke, a_rows)
                                : encode_map(encode, &map_a, L.fmt, L.A, L.M, L.K, L.lda, 64, 64);
-    const bool ok_b = b_kmajor ? encode_map(encode, &map_b, L.fmt, L.B, L.K, L.N, L.ldb, 64, b_rows)
+    const bool ok_b = b_kmajor ? encode_map(encode, &map_b, L.fmt, L.B, L.K, L.N, L.ldb, ke, b_rows)
                                : encode_map(encode, &map_b, L.fmt, L.B, L.N, L.K, L.ldb, 64, 64);
     if (!ok_a || !ok_b) return cudaErrorInvalidValue;
 
@@ -1073,7 +1116,7 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     const int64_t qe = L.swap ? L.M : L.N;
     a.tiles_p = static_cast<int32_t>(ceil_div(pe, L.pair ? 2 * kTcBM : kTcBM));
     a.tiles_q = static_cast<int32_t>(ceil_div(qe, L.bn));
-    a.kb_total = static_cast<int32_t>(ceil_div(L.K, kTcBK));
+    a.kb_total = static_cast<int32_t>(ceil_div(L.K, kind_k_elems(tc_kind(L.fmt))));
     a.splits = L.splits;
     a.kb_per_split = static_cast<int32_t>(ceil_div(a.kb_total, L.splits));
     a.num_units = a.tiles_p * a.tiles_q * L.splits;
@@ -1105,8 +1148,10 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     }
     a.p_kmajor = L.swap ? b_kmajor : a_kmajor;
     a.q_kmajor = L.swap ? a_kmajor : b_kmajor;
-    a.idesc = idesc_f16_f32(static_cast<uint32_t>(L.fmt), !a.p_kmajor, !a.q_kmajor,
-                            L.pair ? 2 * kTcBM : kTcBM, static_cast<uint32_t>(L.bn));
+    // operand format code within the MMA kind
+    const uint32_t fcode = L.fmt == 0 ? 0u : L.fmt == 1 ? 1u : L.fmt == 2 ? 2u : L.fmt == 3 ? 0u : 1u;
+    a.idesc = idesc_f16_f32(fcode, !a.p_kmajor, !a.q_kmajor, L.pair ? 2 * kTcBM : kTcBM,
+                            static_cast<uint32_t>(L.bn));
     a.ws = L.ws;
     a.counters = L.counters;
     a.ab = L.ab;
@@ -1115,25 +1160,10 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
 
     const CUtensorMap& mp = L.swap ? map_b : map_a;
     const CUtensorMap& mq = L.swap ? map_a : map_b;
-    if (L.pair) {
-        switch (L.bn) {
-            case 128: return launch_pair<128>(L, map_a, map_b, map_c, a, stream);
-            case 256: return launch_pair<256>(L, map_a, map_b, map_c, a, stream);
-        }
-        return cudaErrorInvalidValue;
-    }
-    if (!L.swap) {
-        switch (L.bn) {
-            case 64: return launch_cfg<64, false>(L, mp, mq, map_c, a, stream);
-            case 128: return launch_cfg<128, false>(L, mp, mq, map_c, a, stream);
-            case 256: return launch_cfg<256, false>(L, mp, mq, map_c, a, stream);
-        }
-    } else {
-        switch (L.bn) {
-            case 16: return launch_cfg<16, true>(L, mp, mq, map_c, a, stream);
-            case 32: return launch_cfg<32, true>(L, mp, mq, map_c, a, stream);
-            case 64: return launch_cfg<64, true>(L, mp, mq, map_c, a, stream);
-        }
+    switch (tc_kind(L.fmt)) {
+        case 0: return dispatch_kind<0>(L, map_a, map_b, mp, mq, map_c, a, stream);
+        case 1: return dispatch_kind<1>(L, map_a, map_b, mp, mq, map_c, a, stream);
+        case 2: return dispatch_kind<2>(L, map_a, map_b, mp, mq, map_c, a, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -163,7 +163,7 @@ def padded(x: np.ndarray, ld: int) -> np.ndarray:
     if x.dtype == np.float32:
         out[...] = np.float32(1e30)
     elif x.dtype == np.uint8:
-        out[...] = 0x7E     # 448 (E4M3) / 5.7e4 (E5M2): large and finite
+        out[...] = 0x7E     # 448 in E4M3, a NaN in E5M2: either spoils a sum it enters
     else:
         out[...] = 0x7BFF   # large finite in FP16; ~1.1e36 in BF16
     out[:, :cols] = x

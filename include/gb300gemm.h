@@ -102,9 +102,48 @@ gemm_status_t sgemm_f32(const float *A, const float *B, float *C,
                         gemm_stream_t stream);
 
 /*
+ * gemm_tf32f32_bt -- C (FP32) = A x B with FP32 A and B read by the tensor
+ * cores as TF32 (10 fraction bits; the pages' "TF32 path", which changes
+ * results more than any kernel edit -- "matmul_registers.cu", the note on
+ * CUBLAS_COMPUTE_32F), FP32 accumulation.  B is passed TRANSPOSED: Bt is
+ * N x K row-major (ldb >= K), because the tensor cores read TF32 operands
+ * only K-contiguous.  A: M x K row-major.  A and Bt must start on 16-byte
+ * boundaries with lda, ldb multiples of 4; otherwise GEMM_ERR_INVALID_VALUE.
+ * Results stay within (2^-9 + 2^-20) * sum_k |A[i][k]| |B[k][j]| of the exact
+ * product of the FP32 inputs.
+ */
+gemm_status_t gemm_tf32f32_bt(const float *A, const float *Bt, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream);
+
+/*
+ * gemm_e4m3f32_bt / gemm_e5m2f32_bt -- C (FP32) = A x B with 8-bit floating
+ * point A and B (E4M3: 4 exponent bits, 3 fraction bits, largest 448; E5M2:
+ * 5 and 2, largest 57344) on the tensor cores, FP32 accumulation.  The
+ * 8-bit tensor-core modes are the next step the pages point to after 16-bit
+ * inputs ("Tensor cores and matrix operations", "Connections": quantisation
+ * and the 8-bit tensor-core modes).  As for TF32, B is passed TRANSPOSED
+ * (Bt N x K row-major, ldb >= K) and A is M x K row-major; both must start on
+ * 16-byte boundaries with lda, ldb multiples of 16.  Use gemm_ex's alpha for
+ * a scale.
+ */
+gemm_status_t gemm_e4m3f32_bt(const void *A, const void *Bt, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream);
+gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream);
+
+/*
  * Options for gemm_ex.  Zero-initialise and set what you need; a zero field
  * means "let the planner choose".
- *   dtype     0 = FP16, 1 = BF16, 2 = FP32 (sgemm_f32's kernels).
+ *   dtype     0 = FP16, 1 = BF16, 2 = FP32 (sgemm_f32's kernels), 3 = TF32
+ *             (FP32 storage on the tensor cores), 4 = E4M3, 5 = E5M2.  Types
+ *             3-5 need trans_a = 0 and trans_b = 1 (both operands
+ *             K-contiguous) and TMA-legal alignment.
  *   tile_n    dtype 0/1: tensor-core tile width along the MMA's N side: 16,
  *             32, 64, 128 or 256 (16..64 only with swap_ab = 1; 64..256
  *             without).  dtype 2: 128 -> 128x128 SGEMM tiles, 64 -> 128x64,

@@ -7,12 +7,13 @@ import numpy as np
 import oracle
 from dense_gemm_tensor_tcgen05_gb300 import inputs
 
-CODE = {"f16": 0, "bf16": 1, "f32": 2}
+CODE = {"f16": 0, "bf16": 1, "f32": 2, "tf32": 3, "e4m3": 4, "e5m2": 5}
 
 
 def torch_dtype(dt):
     import torch
-    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dt]
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+            "tf32": torch.float32, "e4m3": torch.uint8, "e5m2": torch.uint8}[dt]
 
 
 def to_device(bits: np.ndarray, dt: str, offset_elems: int = 0):
@@ -21,8 +22,10 @@ def to_device(bits: np.ndarray, dt: str, offset_elems: int = 0):
     make misaligned pointers)."""
     import torch
     flat = np.ascontiguousarray(bits).reshape(-1)
-    if dt == "f32":
+    if dt in ("f32", "tf32"):
         host = torch.from_numpy(flat.astype(np.float32, copy=False).view(np.float32))
+    elif dt in ("e4m3", "e5m2"):
+        host = torch.from_numpy(flat.view(np.uint8))
     else:
         host = torch.from_numpy(flat.view(np.int16)).view(torch_dtype(dt))
     if offset_elems:
@@ -58,7 +61,10 @@ def run_gpu(dt, A_bits, B_bits, M, N, K, lda=None, ldb=None, ldc=None, offsets=(
     if opts:
         g.gemm_ex(*args, dtype=CODE[dt], stream=sh, **opts)
     else:
-        {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32}[dt](*args, stream=sh)
+        # tf32/e4m3/e5m2: the _bt entry points (B passed as its N x K transpose)
+        {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32,
+         "tf32": g.gemm_tf32f32_bt, "e4m3": g.gemm_e4m3f32_bt,
+         "e5m2": g.gemm_e5m2f32_bt}[dt](*args, stream=sh)
     g.gemm_device_error(sh)
     tail = Cd[rows * ldc:].cpu().numpy()
     assert np.all(np.isnan(tail)), "kernel wrote past the end of C"
