@@ -387,9 +387,28 @@ def run_suite(g, torch, np, peaks):
             ("bf16", "normal", 8192, 8192, 8192, sig, dict(alpha=0.5, beta=1.0)),
             ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_a=1)),
             ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
-            ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_a=1, trans_b=1))]
-    fns = {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32}
-    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+            ("bf16", "normal", 8192, 8192, 8192, sig, dict(trans_a=1, trans_b=1)),
+            ("tf32", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
+            ("e4m3", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
+            ("e5m2", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
+            ("e4m3", "normal", 16384, 16384, 16384, 1 / 128, dict(trans_b=1))]
+    fns = {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32,
+           "tf32": g.gemm_tf32f32_bt, "e4m3": g.gemm_e4m3f32_bt, "e5m2": g.gemm_e5m2f32_bt}
+    codes = {"f16": 0, "bf16": 1, "f32": 2, "tf32": 3, "e4m3": 4, "e5m2": 5}
+    ebytes = {"f16": 2, "bf16": 2, "f32": 4, "tf32": 4, "e4m3": 1, "e5m2": 1}
+    # tensor-core peak per input type: the measured BF16 figure times the
+    # nominal dense ratio (TF32 1.1, FP8 4.5 against BF16 2.25 PFLOP/s)
+    tc_ratio = {"f16": 1.0, "bf16": 1.0, "tf32": 1.1 / 2.25, "e4m3": 2.0, "e5m2": 2.0}
+    # FP32 on the CUDA cores: 152 SMs x 128 FMA lanes x 2 flops at 2.07 GHz
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+
+    def to_dev(bits, dt):
+        if dt in ("f32", "tf32"):
+            return torch.from_numpy(bits).cuda()
+        if dt in ("e4m3", "e5m2"):
+            return torch.from_numpy(bits.view(np.uint8)).cuda()
+        return torch.from_numpy(bits.view(np.int16)).cuda()
+
     out = []
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
@@ -402,16 +421,15 @@ def run_suite(g, torch, np, peaks):
             A = np.ascontiguousarray(A.T)     # stored K x M
         if tb:
             B = np.ascontiguousarray(B.T)     # stored N x K
-        if dt == "f32":
-            Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
-        else:
-            Ad = torch.from_numpy(A.view(np.int16)).view(tdt[dt]).cuda()
-            Bd = torch.from_numpy(B.view(np.int16)).view(tdt[dt]).cuda()
+        Ad, Bd = to_dev(A, dt), to_dev(B, dt)
+        del A, B
         Cd = torch.zeros((m, n), dtype=torch.float32, device="cuda")
-        code = {"f16": 0, "bf16": 1, "f32": 2}[dt]
+        code = codes[dt]
         lda, ldb = (m if ta else k), (k if tb else n)
         args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), m, n, k, lda, ldb, n)
-        if opts:
+        if code >= 3 and opts == {"trans_b": 1}:
+            call = lambda: fns[dt](*args, sh)     # the _bt entry point
+        elif opts:
             call = lambda: g.gemm_ex(*args, dtype=code, stream=sh, **opts)
         else:
             call = lambda: fns[dt](*args, sh)
@@ -447,14 +465,16 @@ def run_suite(g, torch, np, peaks):
         cold_ms = statistics.median(cold)
         g.gemm_device_error(sh)
         flop = 2.0 * m * n * k
-        byts = (m * k + k * n) * (4 if dt == "f32" else 2) + m * n * 4
+        peak = fp32_peak if dt == "f32" else peaks["bf16_tflops"] * tc_ratio[dt]
+        byts = (m * k + k * n) * ebytes[dt] + m * n * 4
         if opts.get("beta"):
             byts += m * n * 4            # C is read as well
         out.append({"dtype": dt, "M": m, "N": n, "K": k, "options": opts, "plan": plan,
                     "warm_ms": warm_ms, "cold_ms": cold_ms,
                     "tflops_warm": flop / warm_ms / 1e9, "tflops_cold": flop / cold_ms / 1e9,
                     "gbs_warm": byts / warm_ms / 1e6, "gbs_cold": byts / cold_ms / 1e6,
-                    "frac_tc_peak_warm": flop / warm_ms / 1e9 / peaks["bf16_tflops"]})
+                    "peak_tflops": peak,
+                    "frac_peak_warm": flop / warm_ms / 1e9 / peak})
         del Ad, Bd, Cd
         torch.cuda.empty_cache()
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)

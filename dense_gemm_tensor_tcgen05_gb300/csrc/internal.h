@@ -41,6 +41,7 @@ struct TcLaunch {
 // Tile geometry helpers used by the planner and the launcher.
 constexpr int kTcBM = 128;  // rows along the MMA M side (= tensor-memory lanes)
 constexpr int kTcBK = 64;   // k per pipeline stage (64 16-bit elements = 128 bytes)
+constexpr int kPairAtoms = 2;   // 128-byte K atoms per pipeline stage of the CTA-pair kernel
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -58,8 +58,7 @@ constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s for copies already in flight
 constexpr int kThreads = 192;
-constexpr int kUmmaK = 16;
-constexpr int kMmasPerStage = 4;   // each MMA takes 32 of a stage's 128 bytes of K per row
+constexpr int kMmasPerStage = 4;   // MMAs per 128-byte K atom: each takes 32 bytes of K per row
 
 // Elements of K per 128-byte stage row for an MMA kind (0: 16-bit, 1: TF32,
 // 2: 8-bit).
@@ -350,6 +349,20 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, bool kmajor, int
                   : smem_desc_sw128(base + kk * 2048, 8192, 1024);
 }
 
+// The MMA issuer's descriptors, kept in registers: the descriptor of stage s,
+// k-step kk is the stage-0 descriptor plus (s * stage bytes) >> 4 plus
+// kk * step in the start-address field (bits 0-13, address >> 4).  Shared
+// memory addresses stay below 256 KiB, so the sum never carries out of the
+// field, and the issue loop does no descriptor packing and no parameter loads.
+struct DescIter {
+    uint64_t base;   // descriptor of stage 0, k-step 0
+    uint32_t step;   // one k-step in 16-byte units: 32 B (K-major) or 2 KiB (MN-major)
+};
+
+__device__ __forceinline__ DescIter desc_iter(uint32_t base, bool kmajor) {
+    return DescIter{operand_desc(base, kmajor, 0), kmajor ? 2u : 128u};
+}
+
 // ---- TMA-store epilogue ------------------------------------------------------
 //
 // A warp's 32 accumulator rows x 32 columns (one chunk) go through a 4 KiB
@@ -491,6 +504,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            const DescIter dp = desc_iter(smem_base, args.p_kmajor);
+            const DescIter dq = desc_iter(smem_base + T::kPBytes, args.q_kmajor);
+            const uint32_t idesc = args.idesc;
             WorkIter wi(args, blockIdx.x, gridDim.x);
             WorkItem it;
             while (ok && wi.next(args, it)) {
@@ -504,15 +520,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sp = smem_base + stage * T::kStageBytes;
-                    const uint32_t sq = sp + T::kPBytes;
+                    const uint64_t soff = static_cast<uint64_t>((stage * T::kStageBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kMmasPerStage; ++kk) {
-                        const uint64_t adesc = operand_desc(sp, args.p_kmajor, kk);
-                        const uint64_t bdesc = operand_desc(sq, args.q_kmajor, kk);
-                        tc_mma<KIND>(d_tmem, adesc, bdesc, args.idesc,
-                                   (kb > kb0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kMmasPerStage; ++kk)
+                        tc_mma<KIND>(d_tmem, dp.base + soff + kk * dp.step,
+                                     dq.base + soff + kk * dq.step, idesc,
+                                     (kb > kb0 || kk > 0) ? 1u : 0u);
                     tc_commit(empty_bar(stage));   // stage is free once these MMAs finish
                     if (++stage == S) {
                         stage = 0;
@@ -657,17 +670,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
 
 constexpr uint64_t kPairDrainLimitNs = 3 * kWaitLimitNs;
 
+// A stage holds kAtoms 128-byte swizzle atoms along K (each laid out exactly
+// like a one-atom stage, kAtomBytes apart), so the MMA thread issues
+// 4 * kAtoms MMAs per barrier wait and commit.  One thread issuing
+// tcgen05.mma spends tens of cycles per instruction; with one atom per stage
+// the wait, commit and loop overhead of each stage added up to more than the
+// 512 tensor-core cycles the stage's four MMAs take, and the pipe ran dry.
 template <int BN>
 struct PairTraits {
-    static constexpr int kABytes = kTcBM * kTcBK * 2;         // own 128 rows of A
-    static constexpr int kBBytes = (BN / 2) * kTcBK * 2;      // own BN/2 columns of B
+    static constexpr int kAtoms = kPairAtoms;
+    static constexpr int kAAtomBytes = kTcBM * 128;           // own 128 rows of A, one atom
+    static constexpr int kBAtomBytes = (BN / 2) * 128;        // own BN/2 columns of B, one atom
+    static constexpr int kABytes = kAtoms * kAAtomBytes;
+    static constexpr int kBBytes = kAtoms * kBAtomBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = 6;
+    static constexpr int kStoreBytes = kStoreStageBytes;
+    // as many stages as fit beside the store buffers: 3 for BN 256, 4 for BN 128
+    static constexpr int kStages = (227 * 1024 - 2048 - kStoreBytes) / kStageBytes;
     static constexpr int kTmemCols = 2 * BN;
     static constexpr int kNumBars = 2 * kStages + 5;
-    static constexpr int kStoreBytes = kStoreStageBytes;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStoreBytes + kNumBars * 8 + 16;
     static_assert(BN == 256 || BN == 128, "pair tile widths");
+    static_assert(kStages >= 3, "pipeline depth");
     static_assert(kSmemBytes <= 227 * 1024 && kSmemBytes > 114 * 1024, "shared memory");
     static_assert(kTmemCols <= 512, "tensor memory");
 };
@@ -767,12 +791,14 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             bool ok = true;
-            for (int u = cid; ok && u < args.num_units; u += ncl) {
-                int pb, qb, split;
-                unit_coords(args, u, pb, qb, split);
+            WorkIter wi(args, cid, ncl);
+            WorkItem it;
+            while (ok && wi.next(args, it)) {
+                int pb, qb;
+                tile_coords(args, it.tile, pb, qb);
                 const int m0 = pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM;
                 const int n0 = qb * BN + static_cast<int>(rank) * (BN / 2);
-                for (int kb = 0; kb < args.kb_total; ++kb) {
+                for (int ks = it.kb0; ks < it.kb1; ++ks) {
                     if (!pair_wait_phase<false>(empty_bar(stage), phase ^ 1u, wctx, kErrProducer)) {
                         ok = false;
                         break;
@@ -786,9 +812,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     const uint32_t sa = smem_base + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
-                    const int k0 = kb * kind_k_elems(KIND);
-                    load_operand_pair<kTcBM>(sa, &map_a, fb, args.p_kmajor, m0, k0);
-                    load_operand_pair<BN / 2>(sb, &map_b, fb, args.q_kmajor, n0, k0);
+                    // atoms past K are fetched too: the copy fills them with zeros
+#pragma unroll
+                    for (int j = 0; j < T::kAtoms; ++j) {
+                        const int k0 = (ks * T::kAtoms + j) * kind_k_elems(KIND);
+                        load_operand_pair<kTcBM>(sa + j * T::kAAtomBytes, &map_a, fb, args.p_kmajor,
+                                                 m0, k0);
+                        load_operand_pair<BN / 2>(sb + j * T::kBAtomBytes, &map_b, fb, args.q_kmajor,
+                                                  n0, k0);
+                    }
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -808,24 +840,32 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int u = cid; ok && u < args.num_units; u += ncl) {
+            const DescIter da = desc_iter(smem_base, args.p_kmajor);
+            const DescIter db = desc_iter(smem_base + T::kABytes, args.q_kmajor);
+            const uint32_t idesc = args.idesc;
+            WorkIter wi(args, cid, ncl);
+            WorkItem it;
+            while (ok && wi.next(args, it)) {
+                const int kb0 = it.kb0, kb1 = it.kb1;
                 if (!pair_wait_phase<true>(acce_bar(acc), acc_phase ^ 1u, wctx, kErrMma)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < args.kb_total; ++kb) {
+                for (int ks = kb0; ks < kb1; ++ks) {
                     if (!pair_wait_phase<false>(full_bar(stage), phase, wctx, kErrMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = smem_base + stage * T::kStageBytes;
-                    const uint32_t sb = sa + T::kABytes;
+                    const uint64_t soff = static_cast<uint64_t>((stage * T::kStageBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kMmasPerStage; ++kk) {
-                        const uint64_t adesc = operand_desc(sa, args.p_kmajor, kk);
-                        const uint64_t bdesc = operand_desc(sb, args.q_kmajor, kk);
-                        tc_mma_pair<KIND>(d_tmem, adesc, bdesc, args.idesc,
-                                        (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int j = 0; j < T::kAtoms; ++j) {
+                        const uint64_t ao = soff + ((j * T::kAAtomBytes) >> 4);
+                        const uint64_t bo = soff + ((j * T::kBAtomBytes) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < kMmasPerStage; ++kk)
+                            tc_mma_pair<KIND>(d_tmem, da.base + ao + kk * da.step,
+                                              db.base + bo + kk * db.step, idesc,
+                                              (ks > kb0 || j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit_pair_multicast(empty_bar(stage), 0x3);
                     if (++stage == S) {
@@ -848,9 +888,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         StoreStage stg{store_base + static_cast<uint32_t>(warp - 2) * 8192u, 0};
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = cid; u < args.num_units; u += ncl) {
-            int pb, qb, split;
-            unit_coords(args, u, pb, qb, split);
+        WorkIter wi(args, cid, ncl);
+        WorkItem it;
+        while (wi.next(args, it)) {
+            int pb, qb;
+            tile_coords(args, it.tile, pb, qb);
             bool ok = pair_wait_phase<false>(accf_bar(acc), acc_phase, wctx, kErrEpilogue);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) pair_raise_abort(wctx);
@@ -859,8 +901,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             tc_fence_after_sync();
             const uint32_t t_lane = tmem_base + static_cast<uint32_t>(acc * BN) +
                                     (static_cast<uint32_t>(quarter * 32) << 16);
-            const int p = pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM + row;
+            const int row0 = pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM;   // this CTA's rows
+            const int p = row0 + row;
             const int q0 = qb * BN;
+            // A piece of a stream-K tile: each CTA owns its 128 rows of the
+            // workspace slot (tile, piece), laid out [column][row].
+            const bool partial = it.nseg > 1;
+            float* slot = partial
+                ? args.ws + ((static_cast<int64_t>(it.slot) * args.max_seg + it.seg) * 2 + rank) *
+                                (kTcBM * BN)
+                : nullptr;
 #pragma unroll 1
             for (int c = 0; c < BN / CW; ++c) {
                 uint32_t r[CW];
@@ -874,13 +924,52 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 float v[CW];
 #pragma unroll
                 for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
+                if (partial) {
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) slot[(c * CW + i) * kTcBM + row] = v[i];
+                    continue;
+                }
                 apply_ab<false, CW>(args, v, p, q0 + c * CW);
                 if (args.tma_store)
-                    stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
-                                    pb * (2 * kTcBM) + static_cast<int>(rank) * kTcBM + quarter * 32,
-                                    args.M, args.N);
+                    stage_and_store(stg, &map_c, v, lane, q0 + c * CW, row0 + quarter * 32, args.M,
+                                    args.N);
                 else
                     store_chunk<false, CW>(args, v, p, q0 + c * CW);
+            }
+            if (partial) {
+                // the last piece to arrive (per CTA and warp quarter) sums the
+                // pieces in piece order, so results do not depend on timing
+                __threadfence();
+                __syncwarp();
+                uint32_t last = 0;
+                if (lane == 0) {
+                    uint32_t* cnt = args.counters + it.slot * 8 + rank * 4 + quarter;
+                    last = (atomicAdd(cnt, 1u) == static_cast<uint32_t>(it.nseg - 1)) ? 1u : 0u;
+                    if (last) atomicExch(cnt, 0u);   // ready for the next launch
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int c = 0; c < BN / CW; ++c) {
+                        float v[CW];
+#pragma unroll
+                        for (int i = 0; i < CW; ++i) v[i] = 0.0f;
+                        for (int sg = 0; sg < it.nseg; ++sg) {
+                            const float* src =
+                                args.ws + ((static_cast<int64_t>(it.slot) * args.max_seg + sg) * 2 + rank) *
+                                              (kTcBM * BN);
+#pragma unroll
+                            for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
+                        }
+                        apply_ab<false, CW>(args, v, p, q0 + c * CW);
+                        if (args.tma_store)
+                            stage_and_store(stg, &map_c, v, lane, q0 + c * CW, row0 + quarter * 32,
+                                            args.M, args.N);
+                        else
+                            store_chunk<false, CW>(args, v, p, q0 + c * CW);
+                    }
+                }
             }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
@@ -1116,7 +1205,10 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     const int64_t qe = L.swap ? L.M : L.N;
     a.tiles_p = static_cast<int32_t>(ceil_div(pe, L.pair ? 2 * kTcBM : kTcBM));
     a.tiles_q = static_cast<int32_t>(ceil_div(qe, L.bn));
-    a.kb_total = static_cast<int32_t>(ceil_div(L.K, kind_k_elems(tc_kind(L.fmt))));
+    // k-steps: one pipeline stage of K (one 128-byte atom; the pair kernel's
+    // stages hold kPairAtoms)
+    a.kb_total = static_cast<int32_t>(
+        ceil_div(L.K, kind_k_elems(tc_kind(L.fmt)) * (L.pair ? kPairAtoms : 1)));
     a.splits = L.splits;
     a.kb_per_split = static_cast<int32_t>(ceil_div(a.kb_total, L.splits));
     a.num_units = a.tiles_p * a.tiles_q * L.splits;
@@ -1124,7 +1216,6 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.dp_tiles = L.dp_tiles;
     a.sk_kblocks = L.sk_kblocks;
     a.max_seg = L.sk_mode ? L.max_seg : L.splits;
-    if (L.pair && L.sk_mode) return cudaErrorInvalidValue;
     a.group = L.group;
     a.vec_store = ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0 && (L.ldc & 3) == 0) ? 1 : 0;
     // C through TMA stores: FP32 {N, M}, row stride ldc * 4 bytes, box 32 x 32,

@@ -4,8 +4,10 @@
         --K 8192 [--dist normal --sigma 0.011] [--iters 5] [--tile-n 256 --split-k 1 ...]
 
 Inputs are the seeded synthetic matrices of ``inputs.make``; the product runs
-through the C ABI (gemm_f16f32 / gemm_bf16f32 / sgemm_f32, or gemm_ex when
-plan options are given).  Prints the plan and the mean time per call.
+through the C ABI (gemm_f16f32 / gemm_bf16f32 / sgemm_f32 / the _bt entry
+points for tf32, e4m3 and e5m2, or gemm_ex when plan options are given).  For
+tf32, e4m3 and e5m2, B is stored as its N x K transpose.  Prints the plan and
+the mean time per call.
 """
 from __future__ import annotations
 
@@ -15,7 +17,7 @@ import math
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--dtype", choices=["f16", "bf16", "f32"], default="bf16")
+    ap.add_argument("--dtype", choices=["f16", "bf16", "f32", "tf32", "e4m3", "e5m2"], default="bf16")
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)
     ap.add_argument("--K", type=int, default=8192)
@@ -39,27 +41,34 @@ def main():
     sigma = a.sigma or (1 / math.sqrt(a.K) if a.dist == "normal" else 1.0)
     A = inputs.make(a.dist, a.dtype, a.M, a.K, 1, 0, sigma)
     B = inputs.make(a.dist, a.dtype, a.K, a.N, 1, 1, sigma)
-    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[a.dtype]
-    if a.dtype == "f32":
+    code = {"f16": 0, "bf16": 1, "f32": 2, "tf32": 3, "e4m3": 4, "e5m2": 5}[a.dtype]
+    bt = code >= 3
+    if bt:
+        B = np.ascontiguousarray(B.T)
+    if a.dtype in ("f32", "tf32"):
         Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    elif bt:
+        Ad, Bd = torch.from_numpy(A.view(np.uint8)).cuda(), torch.from_numpy(B.view(np.uint8)).cuda()
     else:
-        Ad = torch.from_numpy(A.view(np.int16)).view(tdt).cuda()
-        Bd = torch.from_numpy(B.view(np.int16)).view(tdt).cuda()
+        Ad, Bd = torch.from_numpy(A.view(np.int16)).cuda(), torch.from_numpy(B.view(np.int16)).cuda()
     Cd = torch.empty((a.M, a.N), dtype=torch.float32, device="cuda")
-    code = {"f16": 0, "bf16": 1, "f32": 2}[a.dtype]
     opts = {k: v for k, v in dict(tile_n=a.tile_n, split_k=a.split_k, swap_ab=a.swap_ab,
                                   group_m=a.group_m, cta_pair=a.cta_pair).items()
             if v not in (0, -1)}
-    args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), a.M, a.N, a.K, a.K, a.N, a.N)
+    if bt and opts:
+        opts["trans_b"] = 1
+    args = (Ad.data_ptr(), Bd.data_ptr(), Cd.data_ptr(), a.M, a.N, a.K, a.K,
+            a.K if bt else a.N, a.N)
     s = torch.cuda.current_stream().cuda_stream
     if opts:
         opts.setdefault("swap_ab", -1)
         call = lambda: g.gemm_ex(*args, dtype=code, stream=s, **opts)
         plan = g.gemm_plan_describe(code, *args, **opts)
     else:
-        fn = {0: g.gemm_f16f32, 1: g.gemm_bf16f32, 2: g.sgemm_f32}[code]
+        fn = {0: g.gemm_f16f32, 1: g.gemm_bf16f32, 2: g.sgemm_f32, 3: g.gemm_tf32f32_bt,
+              4: g.gemm_e4m3f32_bt, 5: g.gemm_e5m2f32_bt}[code]
         call = lambda: fn(*args, stream=s)
-        plan = g.gemm_plan_describe(code, *args)
+        plan = g.gemm_plan_describe(code, *args, **({"trans_b": 1} if bt else {}))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     call()
     torch.cuda.synchronize()

@@ -158,8 +158,13 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             256, no swap, no split-K).
  *   store_mode 0 = planner (tensor-core results leave through TMA stores
  *             when C's base, ldc and N allow it), 1 = plain stores.
- *   stream_k  one-CTA tensor-core kernel: 0 = planner (currently off),
- *             1 = off, 2 = on.
+ *   stream_k  0 = planner, 1 = off, 2 = on.  Stream-K keeps whole tiles
+ *             while whole waves last and shares the remaining tiles' K range
+ *             evenly over all CTAs (CTA pairs); a tile cut into pieces is
+ *             summed in a fixed order.  The planner leaves it off (at the
+ *             power cap, idle clusters in a partial last wave let the busy
+ *             ones clock higher, which the measured shapes favour over the
+ *             partial sums' traffic).  Ignored with split_k > 0.
  *   epilogue  0 = C = A x B (alpha and beta ignored); 1 = C = alpha * (A x B)
  *             + beta * C, the accumulate-onto-C form of the tensor-core
  *             operation ("04-wmma-matmul", header comment: D = A*B + C).  The
@@ -174,10 +179,7 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             column-major library ("matmul_registers.cu", the cuBLAS call).
  *             The tensor-core kernels read either layout directly (TMA boxes
  *             and MMA descriptors per layout); FP32 with a transpose runs the
- *             guarded CUDA-core kernel.  gemm_ex_host takes no transposes.  Stream-K keeps
- *             whole tiles while whole waves last and shares the remaining
- *             tiles' k-blocks evenly over all CTAs; a tile cut into pieces
- *             is summed in a fixed order.  Ignored with split_k > 0.
+ *             guarded CUDA-core kernel.  gemm_ex_host takes no transposes.
  * Invalid combinations return GEMM_ERR_INVALID_VALUE.
  */
 typedef struct {

@@ -19,6 +19,7 @@ PLANS = {
     "tc_swap_split_k": ("f16", dict(tile_n=16, swap_ab=1, split_k=4)),
     "tc_stream_k": ("bf16", dict(cta_pair=1, tile_n=64, stream_k=2)),
     "tc_pair": ("bf16", dict(cta_pair=2)),
+    "tc_pair_stream_k": ("f16", dict(cta_pair=2, stream_k=2)),
     "sgemm_128x64": ("f32", dict(tile_n=64)),
     "sgemm_128x128": ("f32", dict(tile_n=128)),
     "sgemm_split": ("f32", dict(tile_n=64, split_k=3)),
@@ -111,3 +112,11 @@ def test_noalloc_with_beta():
     torch.cuda.synchronize()
     R = oracle.gemm_general("f16", A, B, Cin, -1.0, 4.0)
     assert np.array_equal(C.cpu().numpy(), R.astype(np.float32))
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.5, -0.75), (0.5, 0.0)], ids=["ab", "alpha_only_nan_c"])
+def test_general_epilogue_pair_stream_k_cut_tiles(alpha, beta):
+    # the scale and the old C are applied once, by the piece that sums a cut tile
+    _check("bf16", 2560, 2600, 1024, alpha, beta, dict(cta_pair=2, stream_k=2), ldc_pad=4)
+    _check("f16", 2560, 2600, 1024, alpha, beta, dict(cta_pair=2, stream_k=2), dist="small_int",
+           exact=True, seed=2)

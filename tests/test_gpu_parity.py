@@ -287,7 +287,9 @@ MULTI_TILE_PLANS = [dict(cta_pair=1, tile_n=256), dict(cta_pair=1, tile_n=128),
                     dict(cta_pair=2, tile_n=128), dict(cta_pair=1, tile_n=256, store_mode=1),
                     dict(cta_pair=2, tile_n=256, store_mode=1),
                     dict(cta_pair=1, tile_n=256, stream_k=2), dict(cta_pair=1, tile_n=128, stream_k=2),
-                    dict(cta_pair=1, tile_n=256, stream_k=2, store_mode=1)]
+                    dict(cta_pair=1, tile_n=256, stream_k=2, store_mode=1),
+                    dict(cta_pair=2, tile_n=256, stream_k=2), dict(cta_pair=2, tile_n=128, stream_k=2),
+                    dict(cta_pair=2, tile_n=256, stream_k=2, store_mode=1)]
 
 
 @pytest.mark.parametrize("cfg", MULTI_TILE_PLANS, ids=_cfg_id)
@@ -299,6 +301,29 @@ def test_multi_tile_ragged_every_plan(cfg, shape):
     M, N, K = shape
     gu.check_full("f16", "small_int", M, N, K, exact=True, **cfg)
     gu.check_full("bf16", "uniform", M, N, K, seed=4, **cfg)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(2560, 2560, 1024), (2500, 2600, 1000), (1280, 4864, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_cta_pair_stream_k_cut_tiles(dt, shape):
+    # more 256 x 256 tiles than clusters with a partial last wave: tiles are
+    # cut into pieces along K and summed by the last piece to finish
+    M, N, K = shape
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    A, B = gu.make_inputs(dt, "small_int", M, N, K, 0)
+    desc = g.gemm_plan_describe(gu.CODE[dt], 1 << 20, 1 << 34, 1 << 40, M, N, K, K, N, N, cta_pair=2,
+                                stream_k=2)
+    assert "pair=1" in desc and "stream_k" in desc and "max_seg=1 " not in desc, desc
+    C = gu.run_gpu(dt, A, B, M, N, K, cta_pair=2, stream_k=2)
+    assert np.array_equal(C, oracle.gemm(dt, A, B).astype(np.float32))
+
+
+def test_cta_pair_stream_k_on_request_only():
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    args = (1 << 20, 1 << 34, 1 << 40, 8192, 8192, 8192, 8192, 8192, 8192)
+    assert "stream_k" not in g.gemm_plan_describe(1, *args)
+    assert "stream_k" in g.gemm_plan_describe(1, *args, stream_k=2)
 
 
 def test_cta_pair_many_units_per_cluster():
