@@ -42,7 +42,7 @@ import numpy as np
 
 __all__ = [
     "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows", "gemm_general", "gemm_op",
-    "general_bounds", "tf32_bound", "E4M3", "E5M2",
+    "general_bounds", "tf32_bound", "E4M3", "E5M2", "encode16", "round16", "half_ulp16",
     "gemm_entries", "compare", "Comparison", "ABS_COEF", "REL_FROB",
 ]
 
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_e5m2_to_f64.restype = ctypes.c_double
             L.oracle_decode.argtypes = [ctypes.c_int, vp, dp, i64]
             L.oracle_decode.restype = ctypes.c_int
+            L.oracle_encode16.argtypes = [ctypes.c_int, dp, vp, i64]
+            L.oracle_encode16.restype = ctypes.c_int
             L.oracle_gemm_rows.argtypes = [ctypes.c_int, vp, vp, dp, i64, i64, i64,
                                            i64, i64, i64, i64, i64, ctypes.c_int]
             L.oracle_gemm_rows.restype = ctypes.c_int
@@ -162,6 +164,38 @@ def decode(dtype, bits) -> np.ndarray:
     if lib().oracle_decode(code, _ptr(b), _dptr(out), b.size) != 0:
         raise ValueError("oracle_decode failed")
     return out
+
+
+def encode16(dtype, values) -> np.ndarray:
+    """FP16 or BF16 bits (uint16) of float64 values, rounded to nearest, ties
+    to even, by the oracle's own encoder.  Keeps the input's shape."""
+    code = _dtype_code(dtype)
+    if code not in (F16, BF16):
+        raise ValueError("encode16 takes f16 or bf16")
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    if lib().oracle_encode16(code, _dptr(v), _ptr(out), v.size) != 0:
+        raise ValueError("oracle_encode16 failed")
+    return out
+
+
+def round16(dtype, values) -> np.ndarray:
+    """float64 values rounded to FP16 or BF16 (nearest, ties to even) and
+    decoded back: what a 16-bit C holds for an exactly known result."""
+    return decode(dtype, encode16(dtype, values))
+
+
+def half_ulp16(dtype, values) -> np.ndarray:
+    """Half the spacing of FP16 / BF16 numbers at |values|: the largest error
+    of rounding a value of that magnitude to the format (subnormal spacing
+    below the smallest normal)."""
+    code = _dtype_code(dtype)
+    p, emin = (10, -14) if code == F16 else (7, -126)
+    a = np.abs(np.asarray(values, dtype=np.float64))
+    _, E = np.frexp(a)                   # a = m * 2^E, m in [0.5, 1): exponent E - 1
+    e = np.where(a > 0, E - 1, emin)
+    e = np.maximum(e, emin)
+    return np.ldexp(1.0, (e - p - 1).astype(np.int64))
 
 
 def _shape_args(A, B, M, N, K, lda, ldb):

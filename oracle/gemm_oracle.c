@@ -137,6 +137,82 @@ double oracle_e5m2_to_f64(uint8_t x)
     return s ? -v : v;
 }
 
+/* ---- scalar encoders: double -> 16-bit, round to nearest, ties to even ----
+ *
+ * Used only to state what a 16-bit output C should hold: the kernels
+ * accumulate in FP32 and round the result once to FP16 or BF16.  The rounding
+ * is the IEEE-754 default (round to nearest, ties to even), the same rounding
+ * the pages use to make their 16-bit inputs from FP32 values ("04-wmma-matmul",
+ * the __float2half conversion of the host matrices).  Written from the bit
+ * layouts above:
+ *   p fraction bits, exponent bias, smallest normal exponent emin = 1 - bias,
+ *   largest finite exponent emax = bias.
+ * A finite nonzero |x| with binary exponent e (2^e <= |x| < 2^(e+1)) is a
+ * multiple of the quantum q = 2^(max(e, emin) - p) after rounding; |x| / q is
+ * exact in double (a power-of-two scaling), so rounding it to an integer
+ * ties-to-even is exact.  A rounded significand of 2^(p+1) carries into the
+ * exponent; one of 2^p from a subnormal becomes the smallest normal, which
+ * the encoding does by itself (fraction overflow into exponent field 1).
+ * Past the largest finite value the result is infinity.  NaN gives the
+ * format's quiet NaN.                                                       */
+static double round_half_even(double n)
+{
+    double fl = floor(n);
+    double fr = n - fl;                 /* exact: n < 2^53 */
+    if (fr > 0.5)
+        return fl + 1.0;
+    if (fr < 0.5)
+        return fl;
+    return fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;
+}
+
+static uint16_t encode16(double x, int p, int bias, uint16_t qnan)
+{
+    uint16_t sign = (uint16_t)(signbit(x) ? 0x8000u : 0u);
+    if (isnan(x))
+        return qnan;
+    double a = fabs(x);
+    const int emin = 1 - bias, emax = bias;
+    const uint16_t inf = (uint16_t)(((2 * bias + 1) << p));   /* exponent all ones */
+    if (isinf(a))
+        return (uint16_t)(sign | inf);
+    if (a == 0.0)
+        return sign;
+    int E;
+    frexp(a, &E);                       /* a = m * 2^E, m in [0.5, 1) */
+    int e = E - 1;                      /* 2^e <= a < 2^(e+1) */
+    if (e > emax)
+        return (uint16_t)(sign | inf);
+    if (e < emin) {
+        /* subnormal range: quantum 2^(emin - p), exponent field 0 */
+        double r = round_half_even(ldexp(a, p - emin));
+        return (uint16_t)(sign | (uint16_t)r);
+    }
+    double r = round_half_even(ldexp(a, p - e));   /* in [2^p, 2^(p+1)] */
+    if (r == ldexp(1.0, p + 1)) {
+        r = ldexp(1.0, p);
+        e += 1;
+        if (e > emax)
+            return (uint16_t)(sign | inf);
+    }
+    return (uint16_t)(sign | (uint16_t)((e + bias) << p) | (uint16_t)(r - ldexp(1.0, p)));
+}
+
+/* binary16: p = 10, bias 15; bfloat16: p = 7, bias 127. */
+uint16_t oracle_f64_to_f16(double x) { return encode16(x, 10, 15, 0x7e00); }
+uint16_t oracle_f64_to_bf16(double x) { return encode16(x, 7, 127, 0x7fc0); }
+
+/* Encode n doubles to 16-bit (dtype ORACLE_F16 or ORACLE_BF16).  Returns 0,
+ * or -1 on a bad dtype. */
+int oracle_encode16(int dtype, const double *src, uint16_t *dst, int64_t n)
+{
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = dtype == ORACLE_F16 ? oracle_f64_to_f16(src[i]) : oracle_f64_to_bf16(src[i]);
+    return 0;
+}
+
 static double decode_one(int dtype, const void *base, int64_t idx)
 {
     if (dtype == ORACLE_F16)
