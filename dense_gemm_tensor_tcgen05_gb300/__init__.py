@@ -24,7 +24,8 @@ __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
     "gemm_ex_noalloc", "gemm_ex_host", "gemm_plan_describe", "gemm_device_error",
     "gemm_watchdog_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt", "gemm_e5m2f32_bt",
-    "gemm_release_workspace", "gemm_version", "gemm_launch_count", "matmul", "plan", "GemmOptions", "STATUS", "EXPORTED_SYMBOLS",
+    "gemm_release_workspace", "gemm_version", "gemm_launch_count", "matmul", "plan",
+    "GemmOptions", "STATUS", "EXPORTED_SYMBOLS", "C_DTYPE",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,7 +70,7 @@ class GemmOptions(ctypes.Structure):
                 ("stream_k", ctypes.c_int32), ("alpha", ctypes.c_float),
                 ("beta", ctypes.c_float), ("epilogue", ctypes.c_int32),
                 ("trans_a", ctypes.c_int32), ("trans_b", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("c_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -161,10 +162,15 @@ def gemm_e5m2f32_bt(A: int, Bt: int, C: int, M: int, N: int, K: int, lda: int, l
     _check(lib().gemm_e5m2f32_bt(A, Bt, C, M, N, K, lda, ldb, ldc, stream or None))
 
 
+# gemm_options_t.c_dtype codes
+C_DTYPE = {"float32": 0, "float16": 1, "bfloat16": 2}
+
+
 def _options(dtype: int, tile_n=0, split_k=0, swap_ab=-1, generic=0, group_m=0,
              cta_pair=0, store_mode=0, stream_k=0, alpha=None, beta=None, trans_a=0,
-             trans_b=0) -> GemmOptions:
+             trans_b=0, c_dtype=0) -> GemmOptions:
     o = GemmOptions()
+    o.c_dtype = c_dtype
     o.dtype, o.tile_n, o.split_k, o.swap_ab, o.generic, o.group_m = (
         dtype, tile_n, split_k, swap_ab, generic, group_m)
     o.cta_pair, o.store_mode, o.stream_k = cta_pair, store_mode, stream_k
@@ -264,11 +270,13 @@ def _operand_layout(t, name: str):
     raise ValueError(f"{name} must be row-major or column-major")
 
 
-def matmul(A, B, out=None, stream=None, tf32=False, **opts):
+def matmul(A, B, out=None, stream=None, tf32=False, out_dtype=None, **opts):
     """C = A @ B for 2-D tensors (row-major, any row stride).
 
     A and B: both float16, both bfloat16, both float32, both float8_e4m3fn
-    or both float8_e5m2; C is float32.  ``tf32=True`` runs float32 inputs on
+    or both float8_e5m2.  C is float32, or float16 / bfloat16 when ``out``
+    has that dtype or ``out_dtype`` names it (the FP32 result rounded once to
+    nearest even).  ``tf32=True`` runs float32 inputs on
     the tensor cores as TF32.  FP8 and TF32 products need A row-major and B
     column-major (B = Bt.t() for a row-major N x K Bt), on the GPU.
     CUDA tensors run gemm_f16f32 / gemm_bf16f32 / sgemm_f32 (or gemm_ex when
@@ -297,11 +305,19 @@ def matmul(A, B, out=None, stream=None, tf32=False, **opts):
     if K != K2:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     st = stream if stream is not None else torch.cuda.current_stream()
+    c_dt = out.dtype if out is not None else (out_dtype or torch.float32)
+    c_name = str(c_dt).replace("torch.", "")
+    if c_name not in C_DTYPE:
+        raise TypeError(f"C must be float32, float16 or bfloat16, not {c_dt}")
+    if out is not None and out_dtype is not None and out.dtype != out_dtype:
+        raise TypeError("out and out_dtype disagree")
+    if C_DTYPE[c_name]:
+        opts = dict(opts, c_dtype=C_DTYPE[c_name])
     if not A.is_cuda:
         if out is None:
-            out = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
-        elif out.is_cuda or out.dtype != torch.float32 or tuple(out.shape) != (M, N):
-            raise ValueError("out must be a float32 CPU tensor of shape (M, N)")
+            out = torch.empty((M, N), dtype=c_dt, pin_memory=True)
+        elif out.is_cuda or tuple(out.shape) != (M, N):
+            raise ValueError("out must be a CPU tensor of shape (M, N)")
         lda, ldb, ldc = _row_major_ld(A, "A"), _row_major_ld(B, "B"), _row_major_ld(out, "C")
         gemm_ex_host(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc,
                      dtype=code, stream=st.cuda_stream, **opts)
@@ -309,9 +325,9 @@ def matmul(A, B, out=None, stream=None, tf32=False, **opts):
         return out
     if out is None:
         with torch.cuda.stream(st):
-            out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    elif out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
-        raise ValueError("out must be a float32 CUDA tensor of shape (M, N)")
+            out = torch.empty((M, N), dtype=c_dt, device=A.device)
+    elif tuple(out.shape) != (M, N) or not out.is_cuda:
+        raise ValueError("out must be a CUDA tensor of shape (M, N)")
     ldc = _row_major_ld(out, "C")
     ta, lda = _operand_layout(A, "A")
     tb, ldb = _operand_layout(B, "B")
@@ -335,6 +351,8 @@ def matmul(A, B, out=None, stream=None, tf32=False, **opts):
 def plan(A, B, out=None, tf32=False, **opts) -> str:
     """The plan text gemm_plan_describe gives for torch tensors A @ B."""
     code = _code(A)
+    if out is not None and str(out.dtype).replace("torch.", "") in ("float16", "bfloat16"):
+        opts = dict(opts, c_dtype=C_DTYPE[str(out.dtype).replace("torch.", "")])
     if tf32 and code == 2:
         code = 3
     M, K = A.shape

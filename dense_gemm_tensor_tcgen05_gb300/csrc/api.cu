@@ -14,6 +14,7 @@
 #include <utility>
 
 #include "../../include/gb300gemm.h"
+#include "cstore.cuh"
 #include "internal.h"
 
 using namespace gb300;
@@ -185,9 +186,10 @@ bool spans_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
     return a0 < b1 && b0 < a1;
 }
 
-gemm_status_t check_args(const void* A, const void* B, const float* C, int64_t M, int64_t N,
+gemm_status_t check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N,
                          int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int esize,
-                         int trans_a = 0, int trans_b = 0) {
+                         int trans_a = 0, int trans_b = 0, int c_dtype = 0) {
+    if (c_dtype < 0 || c_dtype > 2) return GEMM_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_VALUE;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
     if (trans_a < 0 || trans_a > 1 || trans_b < 0 || trans_b > 1) return GEMM_ERR_INVALID_VALUE;
@@ -204,7 +206,7 @@ gemm_status_t check_args(const void* A, const void* B, const float* C, int64_t M
         (b_rows > 1 && ldb > lim / (b_rows - 1)))
         return GEMM_ERR_INVALID_VALUE;
     const uintptr_t c0 = reinterpret_cast<uintptr_t>(C);
-    const uintptr_t c1 = c0 + static_cast<uintptr_t>((M - 1) * ldc + N) * 4;
+    const uintptr_t c1 = c0 + static_cast<uintptr_t>((M - 1) * ldc + N) * c_elem_bytes(c_dtype);
     if (K > 0) {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(A);
         const uintptr_t a1 = a0 + static_cast<uintptr_t>((a_rows - 1) * lda + a_cols) * esize;
@@ -224,13 +226,14 @@ struct Plan {
     int ab = 0;              // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
     float alpha = 1.0f, beta = 0.0f;
     int trans_a = 0, trans_b = 0;
+    int ct = 0;              // C's type (cstore.cuh)
     TcLaunch tc{};
     SgemmLaunch sg{};
     int64_t units = 0;
     size_t ws_floats = 0, n_counters = 0;
 };
 
-gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64_t M, int64_t N,
+gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_t M, int64_t N,
                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         const gemm_options_t& o, int sms, Plan* plan) {
     Plan p;
@@ -238,6 +241,8 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     if (o.trans_a < 0 || o.trans_a > 1 || o.trans_b < 0 || o.trans_b > 1) return GEMM_ERR_INVALID_VALUE;
     p.trans_a = o.trans_a;
     p.trans_b = o.trans_b;
+    if (o.c_dtype < 0 || o.c_dtype > 2) return GEMM_ERR_INVALID_VALUE;
+    p.ct = o.c_dtype;
     if (o.epilogue) {
         p.alpha = o.alpha;
         p.beta = o.beta;
@@ -253,8 +258,10 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
         return GEMM_OK;
     }
     if (dtype == 2) {
-        const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
-                               reinterpret_cast<uintptr_t>(C)) & 15) == 0 &&
+        // float4 operand loads; C stores of 4 elements (16 bytes FP32, 8 bytes 16-bit)
+        const uintptr_t c_align = p.ct == 0 ? 15 : 7;
+        const bool aligned = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15) == 0 &&
+                             (reinterpret_cast<uintptr_t>(C) & c_align) == 0 &&
                              (lda & 3) == 0 && (ldb & 3) == 0 && (ldc & 3) == 0;
         if (o.generic || !aligned || o.trans_a || o.trans_b) {
             p.kind = Kind::Generic;
@@ -267,6 +274,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
             S.A = static_cast<const float*>(A);
             S.B = static_cast<const float*>(B);
             S.C = C;
+            S.ct = p.ct;
             S.M = M; S.N = N; S.K = K; S.lda = lda; S.ldb = ldb; S.ldc = ldc;
             // 128 x 64 tiles measured faster than 128 x 128 from 2048^3 to
             // 8192 x 8192 x 2048 (3 CTAs of 4 warps per SM against 2 of 8).
@@ -346,6 +354,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, float* C, int64
     L.alpha = p.alpha;
     L.beta = p.beta;
     L.A = A; L.B = B; L.C = C;
+    L.ct = p.ct;
     L.M = M; L.N = N; L.K = K; L.lda = lda; L.ldb = ldb; L.ldc = ldc;
     L.fmt = tc_fmt_of(dtype);
     L.swap = (o.swap_ab < 0) ? ((M <= 64 && N > M) ? 1 : 0) : (o.swap_ab ? 1 : 0);
@@ -500,6 +509,11 @@ void describe(const Plan& p, int dtype, char* buf, int64_t size) {
             snprintf(buf + len, n - len, " epilogue=%s alpha=%g beta=%g",
                      p.ab == 2 ? "alpha*AB+beta*C" : "alpha*AB", p.alpha, p.beta);
     }
+    if (p.ct) {
+        const size_t len = strlen(buf);
+        if (static_cast<int64_t>(len) + 1 < n)
+            snprintf(buf + len, n - len, " c=%s", p.ct == 1 ? "f16" : "bf16");
+    }
 }
 
 void describe_kernel(const Plan& p, int dtype, char* buf, int n) {
@@ -545,12 +559,13 @@ gemm_status_t launch_status(cudaError_t e, const char* what) {
     return GEMM_ERR_LAUNCH;
 }
 
-gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, int64_t N,
+gemm_status_t run(int dtype, const void* A, const void* B, void* C, int64_t M, int64_t N,
                   int64_t K, int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t& o,
                   cudaStream_t stream) {
     if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     const int esize = dtype_bytes(dtype);
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize, o.trans_a, o.trans_b);
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize, o.trans_a, o.trans_b,
+                                  o.c_dtype);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev;
@@ -563,10 +578,10 @@ gemm_status_t run(int dtype, const void* A, const void* B, float* C, int64_t M, 
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;
         case Kind::ZeroFill:   // the empty sum: beta * C, or zeros
-            return launch_status(fill_scale_launch(C, M, N, ldc, p.ab == 2 ? p.beta : 0.0f, stream),
+            return launch_status(fill_scale_launch(C, p.ct, M, N, ldc, p.ab == 2 ? p.beta : 0.0f, stream),
                                  "fill_scale");
         case Kind::Generic:
-            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
+            return launch_status(generic_launch(dtype, A, B, C, p.ct, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
                                                 p.beta, p.trans_a, p.trans_b, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
@@ -622,7 +637,7 @@ gemm_status_t sgemm_f32(const float* A, const float* B, float* C, int64_t M, int
                reinterpret_cast<cudaStream_t>(stream));
 }
 
-static gemm_status_t run_bt(int dtype, const void* A, const void* Bt, float* C, int64_t M,
+static gemm_status_t run_bt(int dtype, const void* A, const void* Bt, void* C, int64_t M,
                             int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                             gemm_stream_t stream) {
     gemm_options_t o = default_options(dtype);
@@ -648,7 +663,7 @@ gemm_status_t gemm_e5m2f32_bt(const void* A, const void* Bt, float* C, int64_t M
     return run_bt(5, A, Bt, C, M, N, K, lda, ldb, ldc, stream);
 }
 
-gemm_status_t gemm_ex(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+gemm_status_t gemm_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t* options,
                       gemm_stream_t stream) {
     if (!options) return GEMM_ERR_INVALID_VALUE;
@@ -656,7 +671,7 @@ gemm_status_t gemm_ex(const void* A, const void* B, float* C, int64_t M, int64_t
                reinterpret_cast<cudaStream_t>(stream));
 }
 
-gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, const float* C,
+gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, const void* C,
                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                  int64_t ldc, const gemm_options_t* options, char* buf,
                                  int64_t size) {
@@ -664,14 +679,14 @@ gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, co
     if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     gemm_options_t o = options ? *options : default_options(dtype);
     gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype_bytes(dtype), o.trans_a,
-                                  o.trans_b);
+                                  o.trans_b, o.c_dtype);
     if (st != GEMM_OK) return st;
     int dev;
     DeviceInfo info;
     st = current_device(&dev, &info);
     if (st != GEMM_OK) return st;
     Plan p;
-    st = make_plan(dtype, A, B, const_cast<float*>(C), M, N, K, lda, ldb, ldc, o, info.sms, &p);
+    st = make_plan(dtype, A, B, const_cast<void*>(C), M, N, K, lda, ldb, ldc, o, info.sms, &p);
     if (st == GEMM_OK) describe(p, dtype, buf, size);
     return st;
 }
@@ -856,7 +871,7 @@ gemm_status_t noalloc_bind_scratch(int dev, const Plan& p, cudaStream_t stream, 
 
 }  // namespace
 
-extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C, int64_t M,
+extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, void* C, int64_t M,
                                          int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                          int64_t ldc, const gemm_options_t* options,
                                          gemm_stream_t stream_handle) {
@@ -864,7 +879,7 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
     const int dtype = options->dtype;
     if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, dtype_bytes(dtype),
-                                  options->trans_a, options->trans_b);
+                                  options->trans_a, options->trans_b, options->c_dtype);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev = 0, sms = 0;
@@ -886,10 +901,10 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, float* C,
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;
         case Kind::ZeroFill:   // the empty sum: beta * C, or zeros
-            return launch_status(fill_scale_launch(C, M, N, ldc, p.ab == 2 ? p.beta : 0.0f, stream),
+            return launch_status(fill_scale_launch(C, p.ct, M, N, ldc, p.ab == 2 ? p.beta : 0.0f, stream),
                                  "fill_scale");
         case Kind::Generic:
-            return launch_status(generic_launch(dtype, A, B, C, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
+            return launch_status(generic_launch(dtype, A, B, C, p.ct, M, N, K, lda, ldb, ldc, p.ab, p.alpha,
                                                 p.beta, p.trans_a, p.trans_b, stream),
                                  "generic_gemm");
         case Kind::Sgemm:
@@ -1011,7 +1026,7 @@ int64_t panel_extent(int64_t n) {
 
 }  // namespace
 
-extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, int64_t M, int64_t N,
+extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int64_t M, int64_t N,
                                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                       const gemm_options_t* options, gemm_stream_t stream_handle) {
     if (!options) return GEMM_ERR_INVALID_VALUE;
@@ -1019,7 +1034,8 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
     if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     const size_t es = dtype_bytes(dtype);
     if (options->trans_a || options->trans_b) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es));
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es), 0, 0,
+                                  options->c_dtype);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     int dev;
@@ -1033,7 +1049,8 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
     // device layouts are dense: ld = K for A panels, N for B and the C panels
     const size_t b_bytes = static_cast<size_t>(std::max<int64_t>(K, 1) * N) * es;
     const size_t a_bytes = static_cast<size_t>(prow * std::max<int64_t>(K, 1)) * es;
-    const size_t c_bytes = static_cast<size_t>(prow * N) * 4;
+    const size_t ces = static_cast<size_t>(c_elem_bytes(options->c_dtype));
+    const size_t c_bytes = static_cast<size_t>(prow * N) * ces;
 
     std::lock_guard<std::mutex> lk(g_hp_mu);
     HostPipe* h = nullptr;
@@ -1080,9 +1097,10 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
                 HP_CHECK(cudaEventRecord(h->e_b, h->s_in), "cudaEventRecord");
                 HP_CHECK(cudaStreamWaitEvent(stream, h->e_b, 0), "cudaStreamWaitEvent");
             }
-            float* cblk = static_cast<float*>(h->dC[buf]) + c0;
+            char* cblk = static_cast<char*>(h->dC[buf]) + c0 * ces;
+            char* chost = static_cast<char*>(C) + (r0 * ldc + c0) * ces;
             if (options->epilogue && options->beta != 0.0f)   // C's old values take part
-                HP_CHECK(cudaMemcpy2DAsync(cblk, N * 4, C + r0 * ldc + c0, ldc * 4, cols * 4, rows,
+                HP_CHECK(cudaMemcpy2DAsync(cblk, N * ces, chost, ldc * ces, cols * ces, rows,
                                            cudaMemcpyHostToDevice, stream),
                          "cudaMemcpy2DAsync(C block in)");
             st = run(dtype, h->dA[buf], static_cast<const char*>(h->dB) + c0 * es, cblk, rows, cols,
@@ -1090,7 +1108,7 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, float* C, in
             if (st != GEMM_OK) return st;
             HP_CHECK(cudaEventRecord(h->e_blk, stream), "cudaEventRecord");
             HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_blk, 0), "cudaStreamWaitEvent");
-            HP_CHECK(cudaMemcpy2DAsync(C + r0 * ldc + c0, ldc * 4, cblk, N * 4, cols * 4, rows,
+            HP_CHECK(cudaMemcpy2DAsync(chost, ldc * ces, cblk, N * ces, cols * ces, rows,
                                        cudaMemcpyDeviceToHost, h->s_out),
                      "cudaMemcpy2DAsync(C block)");
         }

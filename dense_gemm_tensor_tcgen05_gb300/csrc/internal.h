@@ -17,8 +17,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 struct TcLaunch {
     const void* A;
     const void* B;
-    float* C;
+    void* C;            // element type ct
     int64_t M, N, K, lda, ldb, ldc;
+    int ct;         // C's type: 0 = FP32, 1 = FP16, 2 = BF16
     int fmt;        // 0 = FP16, 1 = BF16, 2 = TF32 (FP32 storage), 3 = E4M3, 4 = E5M2
     int bn;         // tile width along the MMA N side
     int swap;       // 1: MMA M side runs along N of C (C^T = B^T A^T)
@@ -92,8 +93,9 @@ struct SgemmPart {
 struct SgemmLaunch {
     const float* A;
     const float* B;
-    float* C;
+    void* C;            // element type ct
     int64_t M, N, K, lda, ldb, ldc;
+    int ct;             // C's type: 0 = FP32, 1 = FP16, 2 = BF16
     int bm, bn;
     int nparts;
     SgemmPart parts[2];
@@ -107,12 +109,12 @@ bool sgemm_tile_supported(int bm, int bn);
 cudaError_t sgemm_blocks_per_sm(int bm, int bn, int* n);
 int sgemm_k_step();
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream);
-cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
+cudaError_t generic_launch(int dtype, const void* A, const void* B, void* C, int ct, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                            int ab, float alpha, float beta, int trans_a, int trans_b,
                            cudaStream_t stream);
 // C = beta * C (scale != 0) or C = 0 (scale == 0, C not read): the K == 0 result.
-cudaError_t fill_scale_launch(float* C, int64_t M, int64_t N, int64_t ldc, float scale,
+cudaError_t fill_scale_launch(void* C, int ct, int64_t M, int64_t N, int64_t ldc, float scale,
                               cudaStream_t stream);
 
 }  // namespace gb300

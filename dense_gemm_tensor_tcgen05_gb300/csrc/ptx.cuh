@@ -106,6 +106,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, fl
                  ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+__device__ __forceinline__ void st_shared_v4_u32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                 uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // ---- tcgen05 ----------------------------------------------------------------
 
 // Allocates `ncols` tensor-memory columns (power of two, 32..512) for this CTA

@@ -25,6 +25,7 @@
 
 #include <cstdio>
 
+#include "cstore.cuh"
 #include "internal.h"
 
 namespace gb300 {
@@ -50,7 +51,7 @@ struct SgemmCfg {
 struct SgArgs {
     const float* A;
     const float* B;
-    float* C;
+    void* C;            // element type ct
     int M, N, K;
     int64_t lda, ldb, ldc;
     int tiles_n;        // tiles along N
@@ -59,6 +60,7 @@ struct SgArgs {
     int k_chunk;        // K per slice, a multiple of BK
     int ab;             // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
     float alpha, beta;
+    int ct;             // C's type (cstore.cuh)
     float* ws;          // split-K partial tiles of this launch
     uint32_t* counters; // split-K arrival counter per tile, zero between launches
 };
@@ -194,7 +196,7 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
         for (int i = 0; i < 4; ++i) {
             const int gm = m0 + qi * (BM / 2) + ty * 4 + i;
             if (EDGE && gm >= a.M) continue;
-            float* crow = a.C + static_cast<int64_t>(gm) * a.ldc;
+            const int64_t crow = static_cast<int64_t>(gm) * a.ldc;
 #pragma unroll
             for (int qj = 0; qj < 2; ++qj) {
                 const int gn = n0 + qj * (BN / 2) + tx * 4;
@@ -206,7 +208,7 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
                 } else if (a.ab == 2) {
                     // alpha * AB + beta * C, reading C only inside it
                     if (!EDGE) {
-                        const float4 c = *reinterpret_cast<const float4*>(crow + gn);
+                        const float4 c = c_load4(a.C, crow + gn, a.ct);
                         v[0] = fmaf(a.alpha, v[0], a.beta * c.x);
                         v[1] = fmaf(a.alpha, v[1], a.beta * c.y);
                         v[2] = fmaf(a.alpha, v[2], a.beta * c.z);
@@ -214,15 +216,16 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            v[j] = fmaf(a.alpha, v[j], (gn + j < a.N) ? a.beta * crow[gn + j] : 0.0f);
+                            v[j] = fmaf(a.alpha, v[j],
+                                        (gn + j < a.N) ? a.beta * c_load(a.C, crow + gn + j, a.ct) : 0.0f);
                     }
                 }
                 if (!EDGE) {
-                    *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
+                    c_store4(a.C, crow + gn, v[0], v[1], v[2], v[3], a.ct);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (gn + j < a.N) crow[gn + j] = v[j];
+                        if (gn + j < a.N) c_store(a.C, crow + gn + j, v[j], a.ct);
                 }
             }
         }
@@ -323,6 +326,7 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
         a.lda = L.lda;
         a.ldb = L.ldb;
         a.ldc = L.ldc;
+        a.ct = L.ct;
         a.tiles_n = static_cast<int>(ceil_div(L.N, BN));
         a.tile0 = part.tile0;
         a.splits = part.splits;
@@ -356,7 +360,7 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return
 // 16, every access guarded: any alignment, any leading dimension.
 template <typename T>
 __global__ void __launch_bounds__(256)
-generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __restrict__ C,
+generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, void* __restrict__ C, int ct,
                     int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc, int ab, float alpha,
                     float beta, int trans_a, int trans_b) {
     __shared__ float As[16][64 + 1];
@@ -402,24 +406,24 @@ generic_gemm_kernel(const T* __restrict__ A, const T* __restrict__ B, float* __r
         for (int j = 0; j < 4; ++j) {
             const int gn = n0 + tx + 16 * j;
             if (gn < N) {
-                float* dst = C + static_cast<int64_t>(gm) * ldc + gn;
+                const int64_t idx = static_cast<int64_t>(gm) * ldc + gn;
                 float v = acc[i][j];
                 if (ab == 1) v *= alpha;
-                else if (ab == 2) v = fmaf(alpha, v, beta * *dst);
-                *dst = v;
+                else if (ab == 2) v = fmaf(alpha, v, beta * c_load(C, idx, ct));
+                c_store(C, idx, v, ct);
             }
         }
     }
 }
 
 // C = scale * C, or C = 0 without reading C when scale == 0.
-__global__ void fill_scale_kernel(float* C, int64_t M, int64_t N, int64_t ldc, float scale) {
+__global__ void fill_scale_kernel(void* C, int ct, int64_t M, int64_t N, int64_t ldc, float scale) {
     const int64_t total = M * N;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / N, c = i - r * N;
-        float* p = C + r * ldc + c;
-        *p = (scale == 0.0f) ? 0.0f : scale * *p;
+        const int64_t idx = r * ldc + c;
+        c_store(C, idx, (scale == 0.0f) ? 0.0f : scale * c_load(C, idx, ct), ct);
     }
 }
 
@@ -451,7 +455,7 @@ cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, int64_t M,
+cudaError_t generic_launch(int dtype, const void* A, const void* B, void* C, int ct, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                            int ab, float alpha, float beta, int trans_a, int trans_b,
                            cudaStream_t stream) {
@@ -460,30 +464,30 @@ cudaError_t generic_launch(int dtype, const void* A, const void* B, float* C, in
     switch (dtype) {
         case 0:
             generic_gemm_kernel<__half><<<grid, 256, 0, stream>>>(
-                static_cast<const __half*>(A), static_cast<const __half*>(B), C, m, n, k, lda, ldb, ldc,
+                static_cast<const __half*>(A), static_cast<const __half*>(B), C, ct, m, n, k, lda, ldb, ldc,
                 ab, alpha, beta, trans_a, trans_b);
             break;
         case 1:
             generic_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-                static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), C, m, n,
+                static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), C, ct, m, n,
                 k, lda, ldb, ldc, ab, alpha, beta, trans_a, trans_b);
             break;
         default:
             generic_gemm_kernel<float><<<grid, 256, 0, stream>>>(
-                static_cast<const float*>(A), static_cast<const float*>(B), C, m, n, k, lda, ldb, ldc,
+                static_cast<const float*>(A), static_cast<const float*>(B), C, ct, m, n, k, lda, ldb, ldc,
                 ab, alpha, beta, trans_a, trans_b);
             break;
     }
     return cudaGetLastError();
 }
 
-cudaError_t fill_scale_launch(float* C, int64_t M, int64_t N, int64_t ldc, float scale,
+cudaError_t fill_scale_launch(void* C, int ct, int64_t M, int64_t N, int64_t ldc, float scale,
                               cudaStream_t stream) {
     const int64_t total = M * N;
     int64_t blocks = ceil_div(total, 256);
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
-    fill_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc, scale);
+    fill_scale_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, ct, M, N, ldc, scale);
     return cudaGetLastError();
 }
 

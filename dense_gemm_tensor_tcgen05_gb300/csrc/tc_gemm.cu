@@ -47,6 +47,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "cstore.cuh"
 #include "ptx.cuh"
 
 namespace gb300 {
@@ -68,7 +69,7 @@ __host__ __device__ constexpr int kind_k_elems(int kind) {
 constexpr int kStoreStageBytes = 4 * 2 * 4096;   // epilogue staging: 4 warps x two 4 KiB buffers
 
 struct TcArgs {
-    float* C;
+    void* C;                    // element type ct
     int64_t ldc;
     int32_t M, N;
     int32_t tiles_p, tiles_q;   // tiles along the MMA M side / N side
@@ -79,7 +80,8 @@ struct TcArgs {
     int64_t sk_kblocks;         // stream-K schedule: k-blocks shared out over the grid
     int32_t max_seg;            // workspace slots per split tile
     int32_t group;
-    int32_t vec_store;          // C rows are 16-byte aligned: float4 stores allowed
+    int32_t ct;                 // C's type: kCF32, kCF16 or kCBF16
+    int32_t vec_store;          // C rows allow 4-element vector accesses (16 B FP32, 8 B 16-bit)
     int32_t tma_store;          // epilogue writes C through the TMA store map
     int32_t ab;                 // 0: C = AB; 1: alpha AB; 2: alpha AB + beta C
     float alpha, beta;
@@ -247,28 +249,27 @@ __device__ __forceinline__ void store_chunk(const TcArgs& a, const float (&v)[W]
     if (!SWAP) {
         // lane = row of C, chunk = W consecutive columns of that row.
         if (p >= a.M) return;
-        float* dst = a.C + static_cast<int64_t>(p) * a.ldc + q0;
+        const int64_t base = static_cast<int64_t>(p) * a.ldc + q0;
         if (a.vec_store && q0 + W <= a.N) {
 #pragma unroll
-            for (int i = 0; i < W; i += 4)
-                *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            for (int i = 0; i < W; i += 4) c_store4(a.C, base + i, v[i], v[i + 1], v[i + 2], v[i + 3], a.ct);
         } else {
 #pragma unroll
             for (int i = 0; i < W; ++i)
-                if (q0 + i < a.N) dst[i] = v[i];
+                if (q0 + i < a.N) c_store(a.C, base + i, v[i], a.ct);
         }
     } else {
         // lane = column of C, chunk = W consecutive rows; lanes of a warp
-        // write 32 consecutive floats of each row.
+        // write 32 consecutive elements of each row.
         if (p >= a.N) return;
-        float* dst = a.C + static_cast<int64_t>(q0) * a.ldc + p;
+        const int64_t base = static_cast<int64_t>(q0) * a.ldc + p;
         if (q0 + W <= a.M) {
 #pragma unroll
-            for (int i = 0; i < W; ++i) dst[static_cast<int64_t>(i) * a.ldc] = v[i];
+            for (int i = 0; i < W; ++i) c_store(a.C, base + static_cast<int64_t>(i) * a.ldc, v[i], a.ct);
         } else {
 #pragma unroll
             for (int i = 0; i < W; ++i)
-                if (q0 + i < a.M) dst[static_cast<int64_t>(i) * a.ldc] = v[i];
+                if (q0 + i < a.M) c_store(a.C, base + static_cast<int64_t>(i) * a.ldc, v[i], a.ct);
         }
     }
 }
@@ -287,11 +288,11 @@ __device__ __forceinline__ void apply_ab(const TcArgs& a, float (&v)[W], int p, 
     }
     if (!SWAP) {
         if (p >= a.M) return;   // never stored
-        const float* src = a.C + static_cast<int64_t>(p) * a.ldc + q0;
+        const int64_t base = static_cast<int64_t>(p) * a.ldc + q0;
         if (a.vec_store && q0 + W <= a.N) {
 #pragma unroll
             for (int i = 0; i < W; i += 4) {
-                const float4 c = *reinterpret_cast<const float4*>(src + i);
+                const float4 c = c_load4(a.C, base + i, a.ct);
                 v[i] = fmaf(alpha, v[i], beta * c.x);
                 v[i + 1] = fmaf(alpha, v[i + 1], beta * c.y);
                 v[i + 2] = fmaf(alpha, v[i + 2], beta * c.z);
@@ -300,14 +301,15 @@ __device__ __forceinline__ void apply_ab(const TcArgs& a, float (&v)[W], int p, 
         } else {
 #pragma unroll
             for (int i = 0; i < W; ++i)
-                v[i] = fmaf(alpha, v[i], (q0 + i < a.N) ? beta * src[i] : 0.0f);
+                v[i] = fmaf(alpha, v[i], (q0 + i < a.N) ? beta * c_load(a.C, base + i, a.ct) : 0.0f);
         }
     } else {
         if (p >= a.N) return;
-        const float* src = a.C + static_cast<int64_t>(q0) * a.ldc + p;
+        const int64_t base = static_cast<int64_t>(q0) * a.ldc + p;
 #pragma unroll
         for (int i = 0; i < W; ++i)
-            v[i] = fmaf(alpha, v[i], (q0 + i < a.M) ? beta * src[static_cast<int64_t>(i) * a.ldc] : 0.0f);
+            v[i] = fmaf(alpha, v[i],
+                        (q0 + i < a.M) ? beta * c_load(a.C, base + static_cast<int64_t>(i) * a.ldc, a.ct) : 0.0f);
     }
 }
 
@@ -377,9 +379,9 @@ struct StoreStage {
     int next;
 };
 
-__device__ __forceinline__ void stage_and_store(StoreStage& st, const CUtensorMap* map_c,
-                                                const float (&v)[32], int lane, int col0, int row0,
-                                                int M, int N) {
+__device__ __forceinline__ void stage_and_store32(StoreStage& st, const CUtensorMap* map_c,
+                                                  const float (&v)[32], int lane, int col0, int row0,
+                                                  int M, int N) {
     const uint32_t buf = st.base + static_cast<uint32_t>(st.next) * 4096u;
     if (lane == 0) bulk_wait_group_read<1>();   // the store issued from this buffer has read it
     __syncwarp();
@@ -400,6 +402,50 @@ __device__ __forceinline__ void stage_and_store(StoreStage& st, const CUtensorMa
         }
         st.next ^= 1;
     }
+}
+
+// 16-bit C: a box is 32 rows x 64 columns (128 bytes a row, the same 4 KiB
+// buffer), filled by two consecutive 32-column chunks -- the even chunk
+// (col0 / 32 even) the row's first 64 bytes, the odd chunk the rest -- and
+// stored after the odd one.  Tile widths are multiples of 64, so chunks come
+// in such pairs.
+__device__ __forceinline__ void stage_and_store16(StoreStage& st, const CUtensorMap* map_c,
+                                                  const float (&v)[32], int lane, int col0, int row0,
+                                                  int M, int N, int ct) {
+    const uint32_t buf = st.base + static_cast<uint32_t>(st.next) * 4096u;
+    const int half = (col0 >> 5) & 1;
+    if (half == 0) {
+        if (lane == 0) bulk_wait_group_read<1>();   // the store issued from this buffer has read it
+        __syncwarp();
+    }
+    const uint32_t rowaddr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t piece = static_cast<uint32_t>(half * 4 + j);
+        st_shared_v4_u32(rowaddr + ((piece ^ static_cast<uint32_t>(lane & 7)) << 4),
+                         c_pack2(v[8 * j], v[8 * j + 1], ct), c_pack2(v[8 * j + 2], v[8 * j + 3], ct),
+                         c_pack2(v[8 * j + 4], v[8 * j + 5], ct), c_pack2(v[8 * j + 6], v[8 * j + 7], ct));
+    }
+    if (half == 0) return;
+    fence_proxy_async_smem();
+    __syncwarp();
+    const int box_col = col0 - 32;
+    if (row0 < M && box_col < N) {
+        if (lane == 0) {
+            tma_store_2d(map_c, buf, box_col, row0);
+            bulk_commit_group();
+        }
+        st.next ^= 1;
+    }
+}
+
+__device__ __forceinline__ void stage_and_store(StoreStage& st, const CUtensorMap* map_c,
+                                                const float (&v)[32], int lane, int col0, int row0,
+                                                int M, int N, int ct) {
+    if (ct == kCF32)
+        stage_and_store32(st, map_c, v, lane, col0, row0, M, N);
+    else
+        stage_and_store16(st, map_c, v, lane, col0, row0, M, N, ct);
 }
 
 // ---- the kernel ---------------------------------------------------------------
@@ -588,7 +634,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     if constexpr (!SWAP) {
                         if (tma_out) {
                             stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
-                                            pb * kTcBM + quarter * 32, args.M, args.N);
+                                            pb * kTcBM + quarter * 32, args.M, args.N, args.ct);
                             continue;
                         }
                     }
@@ -627,7 +673,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                         if constexpr (!SWAP) {
                             if (tma_out) {
                                 stage_and_store(stg, &map_c, v, lane, q0 + c * CW,
-                                                pb * kTcBM + quarter * 32, args.M, args.N);
+                                                pb * kTcBM + quarter * 32, args.M, args.N, args.ct);
                                 continue;
                             }
                         }
@@ -932,7 +978,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 apply_ab<false, CW>(args, v, p, q0 + c * CW);
                 if (args.tma_store)
                     stage_and_store(stg, &map_c, v, lane, q0 + c * CW, row0 + quarter * 32, args.M,
-                                    args.N);
+                                    args.N, args.ct);
                 else
                     store_chunk<false, CW>(args, v, p, q0 + c * CW);
             }
@@ -965,7 +1011,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                         apply_ab<false, CW>(args, v, p, q0 + c * CW);
                         if (args.tma_store)
                             stage_and_store(stg, &map_c, v, lane, q0 + c * CW, row0 + quarter * 32,
-                                            args.M, args.N);
+                                            args.M, args.N, args.ct);
                         else
                             store_chunk<false, CW>(args, v, p, q0 + c * CW);
                     }
@@ -1217,24 +1263,34 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.sk_kblocks = L.sk_kblocks;
     a.max_seg = L.sk_mode ? L.max_seg : L.splits;
     a.group = L.group;
-    a.vec_store = ((reinterpret_cast<uintptr_t>(L.C) & 15) == 0 && (L.ldc & 3) == 0) ? 1 : 0;
-    // C through TMA stores: FP32 {N, M}, row stride ldc * 4 bytes, box 32 x 32,
-    // 128-byte swizzle (needs a 16-byte aligned base and row stride).  The
+    a.ct = L.ct;
+    // 4-element vector accesses: 16 bytes of FP32 or 8 bytes of a 16-bit type
+    const uintptr_t c_addr = reinterpret_cast<uintptr_t>(L.C);
+    const uintptr_t vec_align = L.ct == kCF32 ? 15 : 7;
+    a.vec_store = ((c_addr & vec_align) == 0 && (L.ldc & 3) == 0) ? 1 : 0;
+    // C through TMA stores: {N, M}, row stride ldc * element bytes, 128-byte
+    // swizzle, box 32 x 32 for FP32 and 64 x 32 for 16-bit types (128-byte
+    // rows either way).  Needs a 16-byte aligned base and row stride.  The
     // store clips a box at C's last column only to a 16-byte boundary, so it
-    // is used only when rows end on one (N a multiple of 4): otherwise the
-    // columns between N and the boundary -- the caller's padding -- would be
-    // written.
+    // is used only when rows end on one (N a multiple of 4 FP32 or 8 16-bit
+    // elements): otherwise the columns between N and the boundary -- the
+    // caller's padding -- would be written.
     CUtensorMap map_c;
     memset(&map_c, 0, sizeof(map_c));
     a.tma_store = 0;
-    if (!L.swap && a.vec_store && (L.N % 4) == 0) {
+    const int ces = c_elem_bytes(L.ct);
+    const int64_t row_quantum = 16 / ces;   // elements per 16 bytes
+    if (!L.swap && (c_addr & 15) == 0 && (L.ldc % row_quantum) == 0 && (L.N % row_quantum) == 0) {
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.N), static_cast<cuuint64_t>(L.M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.ldc) * 4};
-        const cuuint32_t box[2] = {32, 32};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.ldc) * ces};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / ces), 32};
         const cuuint32_t estr[2] = {1, 1};
-        if (encode(&map_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, L.C, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+        const CUtensorMapDataType ty = L.ct == kCF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : L.ct == kCF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        if (encode(&map_c, ty, 2, L.C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
             a.tma_store = (L.store_mode == 1) ? 0 : 1;
     }
     a.p_kmajor = L.swap ? b_kmajor : a_kmajor;

@@ -180,6 +180,16 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             The tensor-core kernels read either layout directly (TMA boxes
  *             and MMA descriptors per layout); FP32 with a transpose runs the
  *             guarded CUDA-core kernel.  gemm_ex_host takes no transposes.
+ *   c_dtype   element type of C: 0 = FP32, 1 = FP16, 2 = BF16.  The product
+ *             (and alpha * AB + beta * C) is formed in FP32 as always, then
+ *             rounded once to nearest, ties to even, into the 16-bit C -- the
+ *             16-bit form of the accumulate-onto-C operation the pages
+ *             describe ("Tensor cores and matrix operations": FP16 or FP32
+ *             C and D).  With beta != 0 the old 16-bit C is read and widened
+ *             exactly.  ldc counts elements of C's type; a 16-bit C needs
+ *             only 2-byte alignment (TMA stores are used when its base is
+ *             16-byte aligned and ldc and N are multiples of 8).  Every
+ *             kernel path and gemm_ex_host honour it.
  * Invalid combinations return GEMM_ERR_INVALID_VALUE.
  */
 typedef struct {
@@ -197,11 +207,12 @@ typedef struct {
     int32_t epilogue;
     int32_t trans_a;
     int32_t trans_b;
-    int32_t reserved[2];
+    int32_t c_dtype;
+    int32_t reserved;
 } gemm_options_t;
 
 /* gemm_ex -- the same operation with an explicit plan (tests and tuning). */
-gemm_status_t gemm_ex(const void *A, const void *B, float *C,
+gemm_status_t gemm_ex(const void *A, const void *B, void *C,
                       int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc,
                       const gemm_options_t *options, gemm_stream_t stream);
@@ -213,7 +224,7 @@ gemm_status_t gemm_ex(const void *A, const void *B, float *C,
  * their alignment is read.  Returns the status the call would return from
  * argument checking.
  */
-gemm_status_t gemm_plan_describe(int32_t dtype, const void *A, const void *B, const float *C,
+gemm_status_t gemm_plan_describe(int32_t dtype, const void *A, const void *B, const void *C,
                                  int64_t M, int64_t N, int64_t K,
                                  int64_t lda, int64_t ldb, int64_t ldc,
                                  const gemm_options_t *options, char *buf, int64_t size);
@@ -265,7 +276,7 @@ gemm_status_t gemm_release_workspace(void);
  * one set per (device, stream), allocated on first use and grown as needed;
  * gemm_release_workspace() does not free them.
  */
-gemm_status_t gemm_ex_host(const void *A, const void *B, float *C,
+gemm_status_t gemm_ex_host(const void *A, const void *B, void *C,
                            int64_t M, int64_t N, int64_t K,
                            int64_t lda, int64_t ldb, int64_t ldc,
                            const gemm_options_t *options, gemm_stream_t stream);
@@ -303,7 +314,7 @@ gemm_status_t gemm_ex_host(const void *A, const void *B, float *C,
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
 
-gemm_status_t gemm_ex_noalloc(const void *A, const void *B, float *C,
+gemm_status_t gemm_ex_noalloc(const void *A, const void *B, void *C,
                               int64_t M, int64_t N, int64_t K,
                               int64_t lda, int64_t ldb, int64_t ldc,
                               const gemm_options_t *options, gemm_stream_t stream);
