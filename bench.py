@@ -47,7 +47,7 @@ METRIC = "GEMM TFLOP/s (FP16-in/FP32-acc, M=N=K=8192) and % of GB300 dense peak"
 SEED = 1238
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "tc_gemm_bf16_8192_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "dense_gemm_tensor_tcgen05_gb300", "csrc", f)
-                  for f in ("tc_gemm.cu", "ptx.cuh")]
+                  for f in ("tc_gemm.cu", "ptx.cuh", "cstore.cuh")]
 
 
 def kernel_source_hash() -> str:
@@ -86,8 +86,8 @@ def load_traffic(plan: str):
 
 def kernel_name(plan: str) -> str:
     if "pair=1" in plan:
-        return "tc_gemm_pair_kernel<256> (CTA pairs, 256x256 tiles)"
-    return "tc_gemm_kernel<256,false> (one CTA, 128x256 tiles)"
+        return "tc_gemm_pair_kernel<256, 0> (CTA pairs, 256x256 tiles, 3 stages of 2 K atoms)"
+    return "tc_gemm_kernel<256, false, 0> (one CTA, 128x256 tiles)"
 
 
 # ---- multi-rank aggregation ------------------------------------------------------
@@ -391,7 +391,10 @@ def run_suite(g, torch, np, peaks):
             ("tf32", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
             ("e4m3", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
             ("e5m2", "normal", 8192, 8192, 8192, sig, dict(trans_b=1)),
-            ("e4m3", "normal", 16384, 16384, 16384, 1 / 128, dict(trans_b=1))]
+            ("e4m3", "normal", 16384, 16384, 16384, 1 / 128, dict(trans_b=1)),
+            ("bf16", "normal", 8192, 8192, 8192, sig, dict(c_dtype=2)),
+            ("f16", "normal", 8192, 8192, 8192, sig, dict(c_dtype=1)),
+            ("e4m3", "normal", 8192, 8192, 8192, sig, dict(trans_b=1, c_dtype=2))]
     fns = {"f16": g.gemm_f16f32, "bf16": g.gemm_bf16f32, "f32": g.sgemm_f32,
            "tf32": g.gemm_tf32f32_bt, "e4m3": g.gemm_e4m3f32_bt, "e5m2": g.gemm_e5m2f32_bt}
     codes = {"f16": 0, "bf16": 1, "f32": 2, "tf32": 3, "e4m3": 4, "e5m2": 5}
@@ -466,7 +469,7 @@ def run_suite(g, torch, np, peaks):
         g.gemm_device_error(sh)
         flop = 2.0 * m * n * k
         peak = fp32_peak if dt == "f32" else peaks["bf16_tflops"] * tc_ratio[dt]
-        byts = (m * k + k * n) * ebytes[dt] + m * n * 4
+        byts = (m * k + k * n) * ebytes[dt] + m * n * (2 if opts.get("c_dtype") else 4)
         if opts.get("beta"):
             byts += m * n * 4            # C is read as well
         out.append({"dtype": dt, "M": m, "N": n, "K": k, "options": opts, "plan": plan,

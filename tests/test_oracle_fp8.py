@@ -67,3 +67,20 @@ def test_tf32_bound_covers_truncated_inputs():
     approx = oracle.gemm("f32", trunc(A), trunc(B))
     S = oracle.gemm("f32", np.abs(A), np.abs(B))
     assert np.all(np.abs(approx - exact) <= oracle.tf32_bound(S))
+
+
+def test_tf32_bound_covers_nearest_rounded_inputs():
+    # the other reading: the low 13 fraction bits rounded to nearest (ties to even)
+    A = inputs.uniform_f32(5, 0, (16, 256))
+    B = inputs.uniform_f32(5, 1, (256, 16))
+
+    def rne(x):
+        u = x.view(np.uint32).astype(np.uint64)
+        lsb = (u >> 13) & 1
+        return ((u + 0xFFF + lsb) & 0xFFFFE000).astype(np.uint32).view(np.float32)
+
+    exact = oracle.gemm("f32", A, B)
+    approx = oracle.gemm("f32", rne(A), rne(B))
+    S = oracle.gemm("f32", np.abs(A), np.abs(B))
+    assert np.all(np.abs(approx - exact) <= oracle.tf32_bound(S))
+    assert not np.array_equal(approx, exact)
