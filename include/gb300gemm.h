@@ -1,26 +1,33 @@
 /*
  * gb300gemm.h -- C ABI of the GB300 (sm_103a) dense matrix multiply.
  *
- * Operation (every GEMM entry point): C = A x B, overwriting C, with
+ * Operation: C = A x B, overwriting C, with
  *
  *     C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j]
  *
  * for A of M x K, B of K x N and C of M x N ("Tensor cores and matrix
- * operations", section "Traditional Approach: Element-by-Element").  No
- * alpha, beta or bias.  All three matrices are row-major; a leading
- * dimension is the row stride of the full matrix in elements, not of a tile
- * ("04-wmma-matmul" code example, comment on load_matrix_sync), so element
- * (i, k) of A is A[i * lda + k] and lda >= K, ldb >= N, ldc >= N.
+ * operations", section "Traditional Approach: Element-by-Element").  The
+ * fixed entry points (gemm_f16f32, gemm_bf16f32, sgemm_f32) take row-major
+ * A, B and C and no scaling; gemm_ex and its host and no-alloc forms add,
+ * through gemm_options_t, C = alpha * A x B + beta * C, transposed storage of
+ * A and/or B, and a 16-bit C.  The _bt entry points take B stored as its
+ * transpose.  A leading dimension is the row stride of the full matrix as
+ * stored, in elements, not of a tile ("04-wmma-matmul" code example, comment
+ * on load_matrix_sync): for row-major A element (i, k) is A[i * lda + k] and
+ * lda >= K, ldb >= N, ldc >= N.
  *
  * Arithmetic: the 16-bit entry points multiply FP16 or BF16 inputs and
  * accumulate in FP32 ("CUDA-Practice 09", the sections on mixed precision:
  * 16-bit inputs halve the bytes moved, FP32 accumulation avoids the rounding
  * of long 16-bit sums).  The FP32 entry point computes in FP32 on the CUDA
- * cores ("matmul_registers.cu", the register-tiled SGEMM it builds up).
- * Summation order inside a sum is unspecified; results meet
- * max|C - C_exact| <= 1e-3 sqrt(K) max|A| max|B| and a relative Frobenius
- * error <= 1e-4, and are bit-exact whenever every product and partial sum is
- * an integer below 2^24.
+ * cores ("matmul_registers.cu", the register-tiled SGEMM it builds up).  The
+ * TF32 and FP8 entry points use the tensor cores' TF32 and 8-bit modes with
+ * FP32 accumulation.  Summation order inside a sum is unspecified; FP16,
+ * BF16, FP32 and FP8 results meet max|C - C_exact| <= 1e-3 sqrt(K) max|A|
+ * max|B| and a relative Frobenius error <= 1e-4, and are bit-exact whenever
+ * every product and partial sum is an integer below 2^24 (TF32: see its
+ * entry point).  A 16-bit C holds that FP32 result rounded once to nearest
+ * even.
  *
  * Memory and ownership: A, B and C are DEVICE pointers owned by the caller
  * on the current CUDA device; the library never allocates, frees or copies
@@ -211,18 +218,24 @@ typedef struct {
     int32_t reserved;
 } gemm_options_t;
 
-/* gemm_ex -- the same operation with an explicit plan (tests and tuning). */
+/*
+ * gemm_ex -- the operation with explicit options (gemm_options_t above):
+ * input type, plan, alpha/beta epilogue, transposed storage, C's type.  C is
+ * void* because its element type is options->c_dtype; A and B follow
+ * options->dtype and the trans_* flags.  options must not be NULL.
+ */
 gemm_status_t gemm_ex(const void *A, const void *B, void *C,
                       int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc,
                       const gemm_options_t *options, gemm_stream_t stream);
 
 /*
- * gemm_plan_describe -- the plan gemm_f16f32 / gemm_bf16f32 / sgemm_f32 would
- * use for these arguments on the current device, as text written to buf
- * (always NUL-terminated when size > 0).  Pointers are not dereferenced; only
- * their alignment is read.  Returns the status the call would return from
- * argument checking.
+ * gemm_plan_describe -- the plan gemm_ex would use for these arguments and
+ * options on the current device (options NULL: the plan of the fixed entry
+ * point for `dtype`), as text written to buf (always NUL-terminated when
+ * size > 0).  Pointers are not dereferenced; only their alignment is read.
+ * Returns the status the call would return from argument checking and
+ * planning.
  */
 gemm_status_t gemm_plan_describe(int32_t dtype, const void *A, const void *B, const void *C,
                                  int64_t M, int64_t N, int64_t K,
