@@ -144,23 +144,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Unit -> (tile along MMA M side, tile along MMA N side, K slice).  Tiles are
-// visited in groups of `group` tiles along the M side, column by column, so
-// the CTAs working at one time share operand panels in L2.
-__device__ __forceinline__ void unit_coords(const TcArgs& a, int u, int& pb, int& qb, int& split) {
-    const int tile = u / a.splits;
-    split = u - tile * a.splits;
-    const int group_tiles = a.group * a.tiles_q;
-    const int g = tile / group_tiles;
-    const int first_p = g * a.group;
-    const int gsz = min(a.tiles_p - first_p, a.group);
-    const int r = tile - g * group_tiles;
-    pb = first_p + r % gsz;
-    qb = r / gsz;
-}
-
-// Tile -> (tile along MMA M side, tile along MMA N side), same raster as
-// unit_coords.
+// Tile -> (tile along MMA M side, tile along MMA N side).  Tiles are visited
+// in groups of `group` tiles along the M side, column by column, so the CTAs
+// working at one time share operand panels in L2.
 __device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& pb, int& qb) {
     const int group_tiles = a.group * a.tiles_q;
     const int g = tile / group_tiles;
@@ -169,6 +155,9 @@ __device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& pb, 
     const int r = tile - g * group_tiles;
     pb = first_p + r % gsz;
     qb = r / gsz;
+    // serpentine: odd groups sweep N backwards, so a group starts on the
+    // operand panels the previous group used last (still in L2)
+    if (g & 1) qb = a.tiles_q - 1 - qb;
 }
 
 // One piece of work for a CTA: k-blocks [kb0, kb1) of `tile`.  A tile cut
