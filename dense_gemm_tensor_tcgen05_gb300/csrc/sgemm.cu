@@ -14,7 +14,8 @@
 //   * two shared-memory buffers: the next slice is loaded into registers
 //     while the current one is multiplied, then stored to the other buffer,
 //     with one barrier per K step;
-//   * 64 FFMA per 4 float4 shared loads in the inner loop.
+//   * 64 FMAs per 4 float4 shared loads in the inner loop, issued as 32
+//     packed fma.rn.f32x2 (two FP32 FMAs per instruction).
 // Edges: each CTA decides once whether its tile lies wholly inside C; only
 // boundary tiles use guarded loads and masked stores, and only the last,
 // partial K step of any tile uses guarded loads.  Misaligned pointers or
@@ -138,6 +139,23 @@ __device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs,
     }
 }
 
+// Packed FP32 pairs: fma.rn.f32x2 performs two independent single-rounding
+// FMAs, the same arithmetic as two fmaf, in one instruction -- half the
+// issue slots of the inner loop, which is what bounds this kernel.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ void f32x2_fma(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
 // acc (this thread's 8 x 8 outputs) += A[m0.., kbeg..kend) x B[kbeg..kend, n0..)
 template <int BM, int BN, int BK, bool EDGE>
 __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, int kbeg, int kend,
@@ -147,6 +165,13 @@ __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, 
     const int ty = threadIdx.x / Cfg::kTx;
     const int k_tiles = (kend - kbeg + BK - 1) / BK;
     const int k_full = (kend - kbeg) / BK;   // slices with no K tail
+
+    // accumulators as column pairs (acc[i][2p], acc[i][2p+1])
+    uint64_t acc2[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int p = 0; p < 4; ++p) acc2[i][p] = f32x2_pack(acc[i][2 * p], acc[i][2 * p + 1]);
 
     float4 ra[Cfg::kAPer], rb[Cfg::kBPer];
     sgemm_load<BM, BN, BK, EDGE>(a, m0, n0, kbeg, kend, 0 >= k_full, ra, rb);
@@ -167,11 +192,14 @@ __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, 
             const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * BN + tx * 4);
             const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * BN + BN / 2 + tx * 4);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const uint64_t bp[4] = {f32x2_pack(b0.x, b0.y), f32x2_pack(b0.z, b0.w),
+                                    f32x2_pack(b1.x, b1.y), f32x2_pack(b1.z, b1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+                const uint64_t ai = f32x2_pack(av[i], av[i]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int p = 0; p < 4; ++p) f32x2_fma(acc2[i][p], ai, bp[p]);
+            }
         }
         if (more) {
             float* An = As0 + ((kt + 1) & 1) * (BK * Cfg::kAStride);
@@ -180,6 +208,10 @@ __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, 
         }
         __syncthreads();
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int p = 0; p < 4; ++p) f32x2_unpack(acc2[i][p], acc[i][2 * p], acc[i][2 * p + 1]);
 }
 
 // Quadrant (qi, qj) of the micro-tile: rows m0 + qi*BM/2 + ty*4 + i,
