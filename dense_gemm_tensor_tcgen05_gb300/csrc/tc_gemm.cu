@@ -1,21 +1,23 @@
 // tc_gemm.cu -- persistent, warp-specialised tensor-core GEMM for sm_103a.
 //
-// C (FP32) = A x B with FP16 or BF16 A and B, FP32 accumulation, row-major
-// everything.  The tile decomposition is the one the pages describe for
-// tensor cores -- loop over output tiles, accumulate the tile over K slices,
-// store it once ("Tensor cores and matrix operations", "Complete Algorithm
-// for Large Matrix Multiply") -- mapped onto Blackwell hardware:
+// C = A x B (optionally alpha * A x B + beta * C) with FP16, BF16, TF32 or
+// 8-bit floating-point A and B, FP32 accumulation, C stored as FP32, FP16 or
+// BF16.  The tile decomposition is the one the pages describe for tensor
+// cores -- loop over output tiles, accumulate the tile over K slices, store
+// it once ("Tensor cores and matrix operations", "Complete Algorithm for
+// Large Matrix Multiply") -- mapped onto Blackwell hardware:
 //
-//   * warp 0, one thread: TMA producer.  Per K slice of 64 it loads a
-//     128 x 64 slice of the MMA's A operand and a BN x 64 slice of its B
-//     operand, 128-byte swizzled, into a STAGES-deep shared-memory ring; each
-//     stage has a "full" mbarrier (TMA transaction bytes) and an "empty"
-//     mbarrier (released by the MMA's commit).
+//   * warp 0, one thread: TMA producer.  Per K step -- one 128-byte K atom
+//     (64 16-bit, 32 TF32 or 128 8-bit elements), two in the CTA-pair
+//     kernel -- it loads the rows of the MMA's A and B operands it needs,
+//     128-byte swizzled, into a shared-memory ring; each stage has a "full"
+//     mbarrier (TMA transaction bytes) and an "empty" mbarrier (released by
+//     the MMA's commit).
 //   * warp 1: allocates tensor memory (two BN-column FP32 accumulators of
-//     128 lanes), and one thread issues tcgen05.mma (128 x BN x 16 each, four
-//     per stage) and tcgen05.commit.
+//     128 lanes), and one thread issues tcgen05.mma (four per atom, each
+//     32 bytes of K) and tcgen05.commit.
 //   * warps 2-5: epilogue.  Each warp reads its 32 accumulator lanes with
-//     tcgen05.ld and writes FP32 results to C; the accumulator is double
+//     tcgen05.ld and writes the results to C; the accumulator is double
 //     buffered so the epilogue of one tile overlaps the next tile's main loop.
 //
 // Operand roles.  Without swap, the MMA's A operand is A (K contiguous:
@@ -46,8 +48,8 @@
 #include <cstdio>
 #include <cstring>
 
-#include "internal.h"
 #include "cstore.cuh"
+#include "internal.h"
 #include "ptx.cuh"
 
 namespace gb300 {
