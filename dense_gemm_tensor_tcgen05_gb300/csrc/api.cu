@@ -357,7 +357,8 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
     L.ct = p.ct;
     L.M = M; L.N = N; L.K = K; L.lda = lda; L.ldb = ldb; L.ldc = ldc;
     L.fmt = tc_fmt_of(dtype);
-    L.swap = (o.swap_ab < 0) ? ((M <= 64 && N > M) ? 1 : 0) : (o.swap_ab ? 1 : 0);
+    // swap-AB for small M -- unless CTA pairs were asked for, which never swap
+    L.swap = (o.swap_ab < 0) ? ((M <= 64 && N > M && o.cta_pair != 2) ? 1 : 0) : (o.swap_ab ? 1 : 0);
     if (o.cta_pair < 0 || o.cta_pair > 2) return GEMM_ERR_INVALID_VALUE;
     if (o.store_mode < 0 || o.store_mode > 1) return GEMM_ERR_INVALID_VALUE;
     if (o.stream_k < 0 || o.stream_k > 2) return GEMM_ERR_INVALID_VALUE;

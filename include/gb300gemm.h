@@ -157,7 +157,8 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             32 -> 64x64.
  *   split_k   number of K slices, each reduced in a fixed order (1..64).
  *   swap_ab   -1 = planner, 0 = never, 1 = compute C^T = B^T A^T so that N
- *             runs along the 128-row MMA side (for small M).
+ *             runs along the 128-row MMA side (for small M).  The planner
+ *             never swaps when cta_pair = 2.
  *   generic   1 = force the CUDA-core kernel (any alignment).
  *   group_m   tiles per raster group along the MMA's M side (0 = planner).
  *   cta_pair  0 = planner, 1 = one CTA per 128-row tile, 2 = CTA pairs
