@@ -1072,11 +1072,12 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
     HP_CHECK(cudaEventRecord(h->e_start, stream), "cudaEventRecord");
     HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_start, 0), "cudaStreamWaitEvent");
     HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_start, 0), "cudaStreamWaitEvent");
-    for (int64_t i = 0; i < nrow; ++i) {
+    // A panel i into buffer i % 2, once row panel i - 2 no longer reads it;
+    // `stream` waits for the copy before its next product.
+    auto copy_a = [&](int64_t i) -> gemm_status_t {
         const int buf = static_cast<int>(i & 1);
         const int64_t r0 = i * prow;
         const int64_t rows = std::min<int64_t>(prow, M - r0);
-        // A panel i into buffer `buf`, once row panel i - 2 is no longer read
         if (i >= 2) HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_rowcomp[buf], 0), "cudaStreamWaitEvent");
         if (K > 0)
             HP_CHECK(cudaMemcpy2DAsync(h->dA[buf], K * es, static_cast<const char*>(A) + r0 * lda * es,
@@ -1084,38 +1085,82 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
                      "cudaMemcpy2DAsync(A panel)");
         HP_CHECK(cudaEventRecord(h->e_a, h->s_in), "cudaEventRecord");
         HP_CHECK(cudaStreamWaitEvent(stream, h->e_a, 0), "cudaStreamWaitEvent");
-        // C panel buffer `buf` is free once row panel i - 2 has been copied out
+        // C panel buffer i % 2 is free once row panel i - 2 has been copied out
         if (i >= 2) HP_CHECK(cudaStreamWaitEvent(stream, h->e_rowout[buf], 0), "cudaStreamWaitEvent");
-        for (int64_t j = 0; j < ncol; ++j) {
-            const int64_t c0 = j * pcol;
-            const int64_t cols = std::min<int64_t>(pcol, N - c0);
-            if (i == 0 && K > 0) {
-                // B column panel j, the first time it is needed
-                HP_CHECK(cudaMemcpy2DAsync(static_cast<char*>(h->dB) + c0 * es, N * es,
-                                           static_cast<const char*>(B) + c0 * es, ldb * es,
-                                           cols * es, K, cudaMemcpyHostToDevice, h->s_in),
-                         "cudaMemcpy2DAsync(B panel)");
-                HP_CHECK(cudaEventRecord(h->e_b, h->s_in), "cudaEventRecord");
-                HP_CHECK(cudaStreamWaitEvent(stream, h->e_b, 0), "cudaStreamWaitEvent");
-            }
-            char* cblk = static_cast<char*>(h->dC[buf]) + c0 * ces;
-            char* chost = static_cast<char*>(C) + (r0 * ldc + c0) * ces;
-            if (options->epilogue && options->beta != 0.0f)   // C's old values take part
-                HP_CHECK(cudaMemcpy2DAsync(cblk, N * ces, chost, ldc * ces, cols * ces, rows,
-                                           cudaMemcpyHostToDevice, stream),
-                         "cudaMemcpy2DAsync(C block in)");
-            st = run(dtype, h->dA[buf], static_cast<const char*>(h->dB) + c0 * es, cblk, rows, cols,
-                     K, K, N, N, *options, stream);
-            if (st != GEMM_OK) return st;
-            HP_CHECK(cudaEventRecord(h->e_blk, stream), "cudaEventRecord");
-            HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_blk, 0), "cudaStreamWaitEvent");
-            HP_CHECK(cudaMemcpy2DAsync(chost, ldc * ces, cblk, N * ces, cols * ces, rows,
-                                       cudaMemcpyDeviceToHost, h->s_out),
-                     "cudaMemcpy2DAsync(C block)");
-        }
+        return GEMM_OK;
+    };
+    // B column panel j, copied once; `stream` waits for it before its next product
+    auto copy_b = [&](int64_t j) -> gemm_status_t {
+        if (K == 0) return GEMM_OK;
+        const int64_t c0 = j * pcol;
+        const int64_t cols = std::min<int64_t>(pcol, N - c0);
+        HP_CHECK(cudaMemcpy2DAsync(static_cast<char*>(h->dB) + c0 * es, N * es,
+                                   static_cast<const char*>(B) + c0 * es, ldb * es, cols * es, K,
+                                   cudaMemcpyHostToDevice, h->s_in),
+                 "cudaMemcpy2DAsync(B panel)");
+        HP_CHECK(cudaEventRecord(h->e_b, h->s_in), "cudaEventRecord");
+        HP_CHECK(cudaStreamWaitEvent(stream, h->e_b, 0), "cudaStreamWaitEvent");
+        return GEMM_OK;
+    };
+    // block (i, j): C's old values in (beta != 0), the product on `stream`,
+    // the result out on s_out as soon as it is done
+    auto block = [&](int64_t i, int64_t j) -> gemm_status_t {
+        const int buf = static_cast<int>(i & 1);
+        const int64_t r0 = i * prow, c0 = j * pcol;
+        const int64_t rows = std::min<int64_t>(prow, M - r0);
+        const int64_t cols = std::min<int64_t>(pcol, N - c0);
+        char* cblk = static_cast<char*>(h->dC[buf]) + c0 * ces;
+        char* chost = static_cast<char*>(C) + (r0 * ldc + c0) * ces;
+        if (options->epilogue && options->beta != 0.0f)   // C's old values take part
+            HP_CHECK(cudaMemcpy2DAsync(cblk, N * ces, chost, ldc * ces, cols * ces, rows,
+                                       cudaMemcpyHostToDevice, stream),
+                     "cudaMemcpy2DAsync(C block in)");
+        gemm_status_t bst = run(dtype, h->dA[buf], static_cast<const char*>(h->dB) + c0 * es, cblk,
+                                rows, cols, K, K, N, N, *options, stream);
+        if (bst != GEMM_OK) return bst;
+        HP_CHECK(cudaEventRecord(h->e_blk, stream), "cudaEventRecord");
+        HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_blk, 0), "cudaStreamWaitEvent");
+        HP_CHECK(cudaMemcpy2DAsync(chost, ldc * ces, cblk, N * ces, cols * ces, rows,
+                                   cudaMemcpyDeviceToHost, h->s_out),
+                 "cudaMemcpy2DAsync(C block)");
+        return GEMM_OK;
+    };
+    auto row_done = [&](int64_t i) -> gemm_status_t {
+        const int buf = static_cast<int>(i & 1);
         HP_CHECK(cudaEventRecord(h->e_rowcomp[buf], stream), "cudaEventRecord");
         HP_CHECK(cudaEventRecord(h->e_rowout[buf], h->s_out), "cudaEventRecord");
+        return GEMM_OK;
+    };
+#define HP_TRY(call)                      \
+    do {                                  \
+        gemm_status_t s_ = (call);        \
+        if (s_ != GEMM_OK) return s_;     \
+    } while (0)
+
+    // Row panels 0 and 1 are multiplied together while B streams in: the
+    // copies go A0, B0, A1, B1, B2, ... so the first results -- and the
+    // device-to-host copies, the larger half of the traffic -- start after
+    // two panels instead of after A0 and all of B.
+    const int64_t first = std::min<int64_t>(nrow, 2);
+    HP_TRY(copy_a(0));
+    for (int64_t j = 0; j < ncol; ++j) {
+        HP_TRY(copy_b(j));
+        if (j == 0 && first > 1) {
+            HP_TRY(block(0, 0));
+            HP_TRY(copy_a(1));
+            HP_TRY(block(1, 0));
+            continue;
+        }
+        for (int64_t i = 0; i < first; ++i) HP_TRY(block(i, j));
     }
+    for (int64_t i = 0; i < first; ++i) HP_TRY(row_done(i));
+    // the remaining row panels, one after another, B resident
+    for (int64_t i = 2; i < nrow; ++i) {
+        HP_TRY(copy_a(i));
+        for (int64_t j = 0; j < ncol; ++j) HP_TRY(block(i, j));
+        HP_TRY(row_done(i));
+    }
+#undef HP_TRY
     // later work on `stream` (and the caller's synchronisation) sees all of C
     HP_CHECK(cudaStreamWaitEvent(stream, h->e_rowout[(nrow - 1) & 1], 0), "cudaStreamWaitEvent");
 #undef HP_CHECK

@@ -272,11 +272,12 @@ gemm_status_t gemm_release_workspace(void);
  * gemm_ex_host -- the same operation with A, B and C in HOST memory.
  *
  * The library cuts C into blocks of A row panels by B column panels (up to
- * four of each).  It copies an A panel in, the B panels the first time they
- * are needed, runs each block's product (the kernels of gemm_ex, on
- * `stream`) and copies each C block back as soon as it is done, on two
- * internal copy streams, so the two copy directions overlap each other and
- * the products.
+ * four of each).  It copies the first two A panels in interleaved with the
+ * B panels (A0, B0, A1, B1, B2, ...), the later A panels one by one, runs
+ * each block's product as soon as its panels are in (the kernels of
+ * gemm_ex, on `stream`) and copies each C block back as soon as it is done,
+ * on two internal copy streams, so the two copy directions overlap each
+ * other and the products.
  * With epilogue 1 and beta != 0, each C block is also copied in before its
  * product (on `stream`).
  * For the copies to overlap, A, B and C must be page-locked (cudaHostAlloc /
