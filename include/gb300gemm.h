@@ -40,7 +40,10 @@
  * default stream) and returns without synchronising.  A fault in a kernel
  * surfaces at the caller's next synchronisation; a pipeline wait that ran out
  * of time (see gemm_device_error) is recorded on the device instead of
- * hanging it.
+ * hanging it.  Calls may be captured into a CUDA graph: the plan is fixed at
+ * capture time and the graph replays the same kernels.  A plan with split-K
+ * or stream-K allocates its workspace on its first call, which must
+ * therefore run before the capture (or use gemm_ex_noalloc).
  *
  * Errors: every function returns a gemm_status_t and never prints or exits.
  * Argument errors are found on the host before anything is enqueued.
