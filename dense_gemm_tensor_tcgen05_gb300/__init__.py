@@ -24,7 +24,7 @@ __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
     "gemm_ex_noalloc", "gemm_ex_host", "gemm_plan_describe", "gemm_device_error",
     "gemm_watchdog_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt", "gemm_e5m2f32_bt",
-    "gemm_release_workspace", "gemm_version", "gemm_launch_count", "matmul", "plan",
+    "gemm_release_workspace", "gemm_version", "gemm_launch_count", "matmul", "gemm", "plan",
     "GemmOptions", "STATUS", "EXPORTED_SYMBOLS", "C_DTYPE",
 ]
 
@@ -346,6 +346,11 @@ def matmul(A, B, out=None, stream=None, tf32=False, out_dtype=None, **opts):
     else:
         sgemm_f32(*args, stream=sh)
     return out
+
+
+def gemm(A, B, out=None, **opts):
+    """The same as matmul(A, B, out=out, ...): C = A @ B through the library."""
+    return matmul(A, B, out=out, **opts)
 
 
 def plan(A, B, out=None, tf32=False, **opts) -> str:
