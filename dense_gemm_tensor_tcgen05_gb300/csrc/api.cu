@@ -889,15 +889,6 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, void* C, 
     Plan p;
     st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, *options, sms, &p);
     if (st != GEMM_OK) return st;
-    if (p.kind == Kind::Tc && p.tc.sk_mode && options->stream_k == 0 &&
-        p.ws_floats * sizeof(float) > kNoallocScratchBytes - kNoallocCounterBytes) {
-        // a stream-K schedule the planner chose does not fit the scratch:
-        // whole tiles instead
-        gemm_options_t o = *options;
-        o.stream_k = 1;
-        st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, o, sms, &p);
-        if (st != GEMM_OK) return st;
-    }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;
