@@ -1,7 +1,7 @@
 """Benchmark: BF16-in / FP32-accumulate GEMM, M = N = K = 8192, row-major.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
-                    [--suite]
+                    [--suite [--suite-out PATH]]
 
 One step is one call of gemm_bf16f32 on the M = N = K = 8192 workload (A and
 B drawn from normal(0, 1/sqrt(K)) and rounded to BF16, C in FP32).  A and B
@@ -16,7 +16,8 @@ implementation), on the same workload and metric, each step a bounded sample
 of output rows.
 
 --suite additionally times every workload configuration (not part of the JSON
-line) and writes gpurun_out/bench_suite.json.
+line) and writes them as JSON to --suite-out (default bench_suite.json in the
+working directory).
 
 With torchrun (N > 1) every rank runs its own replica of the workload on its
 own GPU; nothing is exchanged between ranks (the product's rows are
@@ -353,7 +354,7 @@ def run_gb300(args, rank, world, local_rank):
                          f"accumulation, {threads} threads)"}
 
     if args.suite and rank == 0:
-        run_suite(g, torch, np, peaks)
+        run_suite(g, torch, np, peaks, args.suite_out)
 
     if rank == 0:
         line = {
@@ -372,7 +373,7 @@ def run_gb300(args, rank, world, local_rank):
     return 0
 
 
-def run_suite(g, torch, np, peaks):
+def run_suite(g, torch, np, peaks, suite_out):
     """Every workload configuration, timed (not part of the JSON line)."""
     from dense_gemm_tensor_tcgen05_gb300 import inputs
     sig = 1 / math.sqrt(8192)
@@ -480,8 +481,9 @@ def run_suite(g, torch, np, peaks):
                     "frac_peak_warm": flop / warm_ms / 1e9 / peak})
         del Ad, Bd, Cd
         torch.cuda.empty_cache()
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    with open(os.path.join(ROOT, "gpurun_out", "bench_suite.json"), "w") as f:
+    out_dir = os.path.dirname(os.path.abspath(suite_out))
+    os.makedirs(out_dir, exist_ok=True)
+    with open(suite_out, "w") as f:
         json.dump(out, f, indent=1)
     for r in out:
         sys.stderr.write(json.dumps(r) + "\n")
@@ -494,6 +496,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--suite", action="store_true")
+    ap.add_argument("--suite-out", default="bench_suite.json")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
