@@ -278,7 +278,8 @@ def matmul(A, B, out=None, stream=None, tf32=False, out_dtype=None, **opts):
     has that dtype or ``out_dtype`` names it (the FP32 result rounded once to
     nearest even).  ``tf32=True`` runs float32 inputs on
     the tensor cores as TF32.  FP8 and TF32 products need A row-major and B
-    column-major (B = Bt.t() for a row-major N x K Bt), on the GPU.
+    column-major (B = Bt.t() for a row-major N x K Bt).  A and B may each
+    be row-major or column-major (a .t() view), on the GPU or the host.
     CUDA tensors run gemm_f16f32 / gemm_bf16f32 / sgemm_f32 (or gemm_ex when
     plan options are given) on the current (or given) stream and return at
     once.  CPU tensors go through gemm_ex_host -- the library copies them in,
@@ -313,12 +314,18 @@ def matmul(A, B, out=None, stream=None, tf32=False, out_dtype=None, **opts):
         raise TypeError("out and out_dtype disagree")
     if C_DTYPE[c_name]:
         opts = dict(opts, c_dtype=C_DTYPE[c_name])
+    ta, lda = _operand_layout(A, "A")
+    tb, ldb = _operand_layout(B, "B")
+    if code >= 3 and (ta, tb) != (0, 1):
+        raise ValueError("TF32 and FP8 products need A row-major and B column-major")
+    if ta or tb:
+        opts = dict(opts, trans_a=ta, trans_b=tb)
     if not A.is_cuda:
         if out is None:
             out = torch.empty((M, N), dtype=c_dt, pin_memory=True)
         elif out.is_cuda or tuple(out.shape) != (M, N):
             raise ValueError("out must be a CPU tensor of shape (M, N)")
-        lda, ldb, ldc = _row_major_ld(A, "A"), _row_major_ld(B, "B"), _row_major_ld(out, "C")
+        ldc = _row_major_ld(out, "C")
         gemm_ex_host(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc,
                      dtype=code, stream=st.cuda_stream, **opts)
         st.synchronize()
@@ -329,12 +336,6 @@ def matmul(A, B, out=None, stream=None, tf32=False, out_dtype=None, **opts):
     elif tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a CUDA tensor of shape (M, N)")
     ldc = _row_major_ld(out, "C")
-    ta, lda = _operand_layout(A, "A")
-    tb, ldb = _operand_layout(B, "B")
-    if code >= 3 and (ta, tb) != (0, 1):
-        raise ValueError("TF32 and FP8 products need A row-major and B column-major")
-    if ta or tb:
-        opts = dict(opts, trans_a=ta, trans_b=tb)
     args = (A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc)
     sh = st.cuda_stream
     if opts:

@@ -1025,8 +1025,8 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
     const int dtype = options->dtype;
     if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     const size_t es = dtype_bytes(dtype);
-    if (options->trans_a || options->trans_b) return GEMM_ERR_INVALID_VALUE;
-    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es), 0, 0,
+    const int ta = options->trans_a, tb = options->trans_b;
+    gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, static_cast<int>(es), ta, tb,
                                   options->c_dtype);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
@@ -1038,11 +1038,21 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
 
     const int64_t prow = panel_extent(M), pcol = panel_extent(N);
     const int64_t nrow = ceil_div(M, prow), ncol = ceil_div(N, pcol);
-    // device layouts are dense: ld = K for A panels, N for B and the C panels
-    const size_t b_bytes = static_cast<size_t>(std::max<int64_t>(K, 1) * N) * es;
-    const size_t a_bytes = static_cast<size_t>(prow * std::max<int64_t>(K, 1)) * es;
+    // Device copies keep the host layout (A row panels, B column panels, each
+    // stored as the caller stores the matrix), with row strides rounded up to
+    // 16 elements so that every panel is TMA-legal whatever K and N are:
+    //   A panel: rows x K (ld ald), or stored transposed K x rows (ld ald);
+    //   B: K x N (ld bld), or stored transposed N x K (ld bld);
+    //   C panel: rows x N (ld cld).
+    auto up16 = [](int64_t x) { return std::max<int64_t>(ceil_div(x, 16) * 16, 16); };
+    const int64_t Kp = std::max<int64_t>(K, 1);
+    const int64_t ald = ta ? up16(prow) : up16(K);
+    const int64_t bld = tb ? up16(K) : up16(N);
+    const int64_t cld = up16(N);
+    const size_t a_bytes = static_cast<size_t>((ta ? Kp : prow) * ald) * es;
+    const size_t b_bytes = static_cast<size_t>((tb ? N : Kp) * bld) * es;
     const size_t ces = static_cast<size_t>(c_elem_bytes(options->c_dtype));
-    const size_t c_bytes = static_cast<size_t>(prow * N) * ces;
+    const size_t c_bytes = static_cast<size_t>(prow * cld) * ces;
 
     std::lock_guard<std::mutex> lk(g_hp_mu);
     HostPipe* h = nullptr;
@@ -1070,9 +1080,13 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
         const int64_t r0 = i * prow;
         const int64_t rows = std::min<int64_t>(prow, M - r0);
         if (i >= 2) HP_CHECK(cudaStreamWaitEvent(h->s_in, h->e_rowcomp[buf], 0), "cudaStreamWaitEvent");
-        if (K > 0)
-            HP_CHECK(cudaMemcpy2DAsync(h->dA[buf], K * es, static_cast<const char*>(A) + r0 * lda * es,
+        if (K > 0 && !ta)
+            HP_CHECK(cudaMemcpy2DAsync(h->dA[buf], ald * es, static_cast<const char*>(A) + r0 * lda * es,
                                        lda * es, K * es, rows, cudaMemcpyHostToDevice, h->s_in),
+                     "cudaMemcpy2DAsync(A panel)");
+        if (K > 0 && ta)   // columns r0.. of the stored K x M matrix
+            HP_CHECK(cudaMemcpy2DAsync(h->dA[buf], ald * es, static_cast<const char*>(A) + r0 * es,
+                                       lda * es, rows * es, K, cudaMemcpyHostToDevice, h->s_in),
                      "cudaMemcpy2DAsync(A panel)");
         HP_CHECK(cudaEventRecord(h->e_a, h->s_in), "cudaEventRecord");
         HP_CHECK(cudaStreamWaitEvent(stream, h->e_a, 0), "cudaStreamWaitEvent");
@@ -1085,10 +1099,16 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
         if (K == 0) return GEMM_OK;
         const int64_t c0 = j * pcol;
         const int64_t cols = std::min<int64_t>(pcol, N - c0);
-        HP_CHECK(cudaMemcpy2DAsync(static_cast<char*>(h->dB) + c0 * es, N * es,
-                                   static_cast<const char*>(B) + c0 * es, ldb * es, cols * es, K,
-                                   cudaMemcpyHostToDevice, h->s_in),
-                 "cudaMemcpy2DAsync(B panel)");
+        if (!tb)
+            HP_CHECK(cudaMemcpy2DAsync(static_cast<char*>(h->dB) + c0 * es, bld * es,
+                                       static_cast<const char*>(B) + c0 * es, ldb * es, cols * es, K,
+                                       cudaMemcpyHostToDevice, h->s_in),
+                     "cudaMemcpy2DAsync(B panel)");
+        else   // rows c0.. of the stored N x K matrix
+            HP_CHECK(cudaMemcpy2DAsync(static_cast<char*>(h->dB) + c0 * bld * es, bld * es,
+                                       static_cast<const char*>(B) + c0 * ldb * es, ldb * es, K * es, cols,
+                                       cudaMemcpyHostToDevice, h->s_in),
+                     "cudaMemcpy2DAsync(B panel)");
         HP_CHECK(cudaEventRecord(h->e_b, h->s_in), "cudaEventRecord");
         HP_CHECK(cudaStreamWaitEvent(stream, h->e_b, 0), "cudaStreamWaitEvent");
         return GEMM_OK;
@@ -1103,15 +1123,16 @@ extern "C" gemm_status_t gemm_ex_host(const void* A, const void* B, void* C, int
         char* cblk = static_cast<char*>(h->dC[buf]) + c0 * ces;
         char* chost = static_cast<char*>(C) + (r0 * ldc + c0) * ces;
         if (options->epilogue && options->beta != 0.0f)   // C's old values take part
-            HP_CHECK(cudaMemcpy2DAsync(cblk, N * ces, chost, ldc * ces, cols * ces, rows,
+            HP_CHECK(cudaMemcpy2DAsync(cblk, cld * ces, chost, ldc * ces, cols * ces, rows,
                                        cudaMemcpyHostToDevice, stream),
                      "cudaMemcpy2DAsync(C block in)");
-        gemm_status_t bst = run(dtype, h->dA[buf], static_cast<const char*>(h->dB) + c0 * es, cblk,
-                                rows, cols, K, K, N, N, *options, stream);
+        const char* bblk = static_cast<const char*>(h->dB) + (tb ? c0 * bld : c0) * es;
+        gemm_status_t bst = run(dtype, h->dA[buf], bblk, cblk, rows, cols, K, ald, bld, cld,
+                                *options, stream);
         if (bst != GEMM_OK) return bst;
         HP_CHECK(cudaEventRecord(h->e_blk, stream), "cudaEventRecord");
         HP_CHECK(cudaStreamWaitEvent(h->s_out, h->e_blk, 0), "cudaStreamWaitEvent");
-        HP_CHECK(cudaMemcpy2DAsync(chost, ldc * ces, cblk, N * ces, cols * ces, rows,
+        HP_CHECK(cudaMemcpy2DAsync(chost, ldc * ces, cblk, cld * ces, cols * ces, rows,
                                    cudaMemcpyDeviceToHost, h->s_out),
                  "cudaMemcpy2DAsync(C block)");
         return GEMM_OK;

@@ -190,7 +190,7 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             column-major library ("matmul_registers.cu", the cuBLAS call).
  *             The tensor-core kernels read either layout directly (TMA boxes
  *             and MMA descriptors per layout); FP32 with a transpose runs the
- *             guarded CUDA-core kernel.  gemm_ex_host takes no transposes.
+ *             guarded CUDA-core kernel.  gemm_ex_host honours both flags.
  *   c_dtype   element type of C: 0 = FP32, 1 = FP16, 2 = BF16.  The product
  *             (and alpha * AB + beta * C) is formed in FP32 as always, then
  *             rounded once to nearest, ties to even, into the 16-bit C -- the
@@ -285,7 +285,13 @@ gemm_status_t gemm_release_workspace(void);
  * product (on `stream`).
  * For the copies to overlap, A, B and C must be page-locked (cudaHostAlloc /
  * cudaHostRegister); pageable memory works but serialises.  Leading
- * dimensions are those of the host arrays.
+ * dimensions are those of the host arrays.  With trans_a, an A panel is a
+ * column block of the stored K x M matrix; with trans_b, a B panel is a row
+ * block of the stored N x K matrix (so TF32 and the 8-bit types, which take
+ * B transposed, run from host buffers too).  The device copies keep each
+ * operand's storage order with row strides rounded up to 16 elements, so
+ * every panel suits the TMA kernels whatever the host leading dimensions
+ * are (the rules on lda and ldb above apply to the host arrays only).
  *
  * The call returns after enqueueing; C is complete when `stream` reaches
  * this point (synchronise `stream` before reading C).  Work already queued on

@@ -86,21 +86,29 @@ def _run(dt, M, N, K, o, c_dtype, pad, seed, entry="ex"):
     ldb = -(-Bs.shape[1] // align) * align + (align if pad else 0)
     As, Bs = inputs.padded(As, lda), inputs.padded(Bs, ldb)
     ldc = N + pad
-    Ad, Bd = gu.to_device(As, dt), gu.to_device(Bs, dt)
+    host = entry == "host"
+    if host:   # page-locked host buffers: the library stages them itself
+        Ad, Bd = gu.to_device(As, dt).cpu().pin_memory(), gu.to_device(Bs, dt).cpu().pin_memory()
+    else:
+        Ad, Bd = gu.to_device(As, dt), gu.to_device(Bs, dt)
+    dev = "cpu" if host else "cuda"
     guard = 4096
     cin = ((np.arange(M * ldc).reshape(M, ldc) % 7) - 3).astype(np.float64)
     if c_dtype == 0:
-        cbuf = torch.full((M * ldc + guard,), float("nan"), dtype=torch.float32, device="cuda")
+        cbuf = torch.full((M * ldc + guard,), float("nan"), dtype=torch.float32, device=dev)
         cbuf[: M * ldc] = torch.from_numpy(cin.astype(np.float32).ravel())
     else:
         cbuf = torch.full((M * ldc + guard,), int(np.uint16(NAN16[c_dtype]).view(np.int16)),
-                          dtype=torch.int16, device="cuda")
+                          dtype=torch.int16, device=dev)
         cbits = oracle.encode16(C_NAMES[c_dtype], cin)
         cbuf[: M * ldc] = torch.from_numpy(cbits.view(np.int16).ravel())
+    if host:
+        cbuf = cbuf.pin_memory()
     s = torch.cuda.current_stream().cuda_stream
-    call = g.gemm_ex if entry == "ex" else g.gemm_ex_noalloc
+    call = {"ex": g.gemm_ex, "noalloc": g.gemm_ex_noalloc, "host": g.gemm_ex_host}[entry]
     call(Ad.data_ptr(), Bd.data_ptr(), cbuf.data_ptr(), M, N, K, lda, ldb, ldc,
          dtype=gu.CODE[dt], stream=s, c_dtype=c_dtype, **o)
+    torch.cuda.current_stream().synchronize()
     g.gemm_device_error(s)
     out = cbuf.cpu().numpy()
     if c_dtype:
@@ -141,3 +149,12 @@ def test_fuzz_case_noalloc(case):
     # scratch holds every split-K / stream-K workspace these shapes need)
     dt, M, N, K, o, c_dtype, pad = CASES[case]
     _run(dt, M, N, K, o, c_dtype, pad, seed=case, entry="noalloc")
+
+
+@pytest.mark.parametrize("case", range(1, N_CASES, 4))
+def test_fuzz_case_host(case):
+    # other cases through the host-buffer entry point (page-locked A, B, C);
+    # its staging copies pad the leading dimensions, so the plan options act
+    # on panels of the same shapes with other strides
+    dt, M, N, K, o, c_dtype, pad = CASES[case]
+    _run(dt, M, N, K, o, c_dtype, pad, seed=case, entry="host")
