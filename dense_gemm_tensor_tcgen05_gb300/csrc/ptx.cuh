@@ -1,6 +1,6 @@
 // ptx.cuh -- inline-PTX wrappers for the sm_103a features the tensor-core
-// GEMM uses: mbarriers, TMA tensor copies and the tcgen05 family (tensor
-// memory allocation, MMA, commit, loads, fences).  Each wrapper is one PTX
+// GEMM uses: mbarriers, TMA tensor copies, programmatic dependent launch and
+// the tcgen05 family (tensor memory allocation, MMA, commit, loads, fences).  Each wrapper is one PTX
 // instruction (or a tiny fixed sequence) from the public PTX ISA.
 #pragma once
 
@@ -17,6 +17,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+//
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel on its stream is still running.  griddepcontrol.wait
+// blocks until that kernel has completed and its memory operations are
+// visible; launch_dependents lets the next such kernel on the stream start
+// (once every CTA of this grid has issued it or exited).
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- mbarrier -------------------------------------------------------------

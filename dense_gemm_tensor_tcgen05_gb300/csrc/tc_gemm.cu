@@ -39,6 +39,15 @@
 // the quarter that arrives last sums the partials in slice order 0..S-1 (a
 // fixed order, so results do not depend on timing) and writes C.
 //
+// Back-to-back launches.  Both kernels are launched with programmatic stream
+// serialization: a launch may start while the previous kernel on the stream
+// is still finishing, runs its prologue (barrier set-up, tensor-memory
+// allocation, tensor-map prefetch) on the SMs that kernel has left, and
+// waits (griddepcontrol.wait) for it to complete before its first global
+// memory access.  A stream of GEMMs then hides most of each launch's
+// start-up; the order of every read and write of global memory is the same
+// as with plain launches.
+//
 // Waits.  Every mbarrier wait gives up after kWaitLimitNs, sets a bit in the
 // device error word and makes the whole CTA leave its loops; before exiting,
 // the producer waits (bounded) for its own TMA copies and the MMA thread for
@@ -493,6 +502,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touches only this CTA's shared and tensor memory, so
+    // it may overlap the previous kernel on the stream; every global access
+    // below comes after that kernel has finished.
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const WaitCtx wctx{abort_flag};
 
     if (warp == 0) {
@@ -816,6 +830,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     cluster_sync();   // both CTAs' barriers exist and tensor memory is allocated
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touches only this CTA's shared and tensor memory, so
+    // it may overlap the previous kernel on the stream; every global access
+    // below comes after that kernel has finished.
+    grid_dep_launch_dependents();
+    grid_dep_wait();
     const PairWaitCtx wctx{abort_flag,
                            mapa_shared(smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u)};
     const int cid = static_cast<int>(cluster_id_x());
@@ -1110,8 +1129,10 @@ static cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchA
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
@@ -1121,7 +1142,7 @@ static cudaError_t pair_max_clusters_for(int* n) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PairTraits<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config<BN>(2, nullptr, attr);
     return cudaOccupancyMaxActiveClusters(n, kern, &cfg);
 }
@@ -1168,8 +1189,17 @@ static cudaError_t launch_cfg(const TcLaunch& L, const CUtensorMap& mp, const CU
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, kThreads, T::kSmemBytes, stream>>>(mp, mq, mc, args);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mp, mq, mc, args);
 }
 
 template <int BN, int KIND>
@@ -1179,7 +1209,7 @@ static cudaError_t launch_pair(const TcLaunch& L, const CUtensorMap& ma, const C
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PairTraits<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config<BN>(L.grid, stream, attr);
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, args);
 }
