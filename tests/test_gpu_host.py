@@ -121,3 +121,12 @@ def test_matmul_host_views():
     C8 = g.matmul(a8, b8.t(), out_dtype=torch.bfloat16)
     R8 = oracle.gemm_op("e4m3", 0, 1, A8, np.ascontiguousarray(B8.T), M, N, K)
     assert np.array_equal(C8.view(torch.int16).numpy().view(np.uint16), oracle.encode16("bf16", R8))
+
+
+@pytest.mark.parametrize("case", [("f16", 0, 0, None, None), ("bf16", 1, 1, 1.5, -0.75),
+                                  ("e4m3", 0, 1, 2.0, 0.5), ("f32", 1, 0, 0.5, 0.0)],
+                         ids=lambda c: "-".join(map(str, c)))
+def test_host_empty_k(case):
+    # K = 0: nothing is copied in but C's old values (beta != 0); C = beta * C or 0
+    dt, ta, tb, alpha, beta = case
+    _host_case(dt, 1300, 1100, 0, ta, tb, pad=4, alpha=alpha, beta=beta, seed=7)
