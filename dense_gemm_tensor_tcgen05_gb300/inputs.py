@@ -188,12 +188,18 @@ def make(dist: str, dtype: str, rows: int, cols: int, seed: int, matrix_id: int,
     elif dist == "normal":
         x = normal_f32(seed, matrix_id, (rows, cols), sigma)
     elif dist == "small_int":
+        # (r + 2c) mod 7 and (3r + c) mod 5 depend on c only through c mod 7
+        # (mod 5): round one period per row to the element type, then repeat
+        # its bits along the row (the same bits as rounding every element)
         r = np.arange(rows, dtype=np.int64)[:, None]
-        c = np.arange(cols, dtype=np.int64)[None, :]
+        p = 7 if matrix_id == 0 else 5
+        c = np.arange(p, dtype=np.int64)[None, :]
         if matrix_id == 0:
-            x = ((r + 2 * c) % 7 - 3).astype(np.float32)
+            period = ((r + 2 * c) % 7 - 3).astype(np.float32)
         else:
-            x = ((3 * r + c) % 5 - 2).astype(np.float32)
+            period = ((3 * r + c) % 5 - 2).astype(np.float32)
+        bits = to_bits(period, dtype)
+        return np.ascontiguousarray(np.take(bits, np.arange(cols, dtype=np.int64) % p, axis=1))
     elif dist == "mod_pattern":
         i = np.arange(rows * cols, dtype=np.int64)
         if matrix_id == 0:
