@@ -445,9 +445,8 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
         // Stream-K: whole tiles while whole waves last, then the remaining
         // tiles' k-blocks shared evenly by every CTA (partial tiles summed in
         // a fixed order), so no SM idles through a partial last wave.  Opt-in:
-        // on the measured shapes the sum of a split tile's pieces, one L2 round
-        // trip per 32-column chunk and piece, costs more than the idle SMs
-        // of the last wave.
+        // on the measured shapes it is slower than whole tiles, and a variant
+        // that moves no partial sums at all is still no faster.
         const int64_t slot_tiles = tc_streamk_schedule(L, tiles, kb_total, sms);
         p.units = tiles;
         if (slot_tiles > 0) {
