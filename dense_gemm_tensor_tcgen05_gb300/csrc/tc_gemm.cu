@@ -240,6 +240,40 @@ struct WorkIter {
     }
 };
 
+// ---- split tiles ---------------------------------------------------------------
+//
+// A piece of a split tile is stored [column][row] (kTcBM rows a column), so
+// a warp's loads and stores of one column are 32 consecutive floats.  The
+// sum of a chunk of W columns over the n pieces is taken in piece order
+// 0..n-1 (results do not depend on timing).  The loads of P pieces are
+// issued before any is added, so a chunk costs one L2 round trip per P
+// pieces instead of one per piece; callers pick P so that the P x W values
+// fit in registers beside the rest of their epilogue.
+template <int W, int P>
+__device__ __forceinline__ void sum_pieces(float (&v)[W], const float* piece0, int n,
+                                           int64_t piece_stride, int col0, int row) {
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] = 0.0f;
+    for (int s0 = 0; s0 < n; s0 += P) {
+        float t[P][W];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            if (s0 + j < n) {
+                const float* src = piece0 + static_cast<int64_t>(s0 + j) * piece_stride;
+#pragma unroll
+                for (int i = 0; i < W; ++i) t[j][i] = __ldcg(src + (col0 + i) * kTcBM + row);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+            if (s0 + j < n) {
+#pragma unroll
+                for (int i = 0; i < W; ++i) v[i] += t[j][i];
+            }
+        }
+    }
+}
+
 // ---- epilogue stores ----------------------------------------------------------
 
 // W accumulator values of this thread's lane (`p` along the MMA M side),
@@ -667,13 +701,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
 #pragma unroll 1
                     for (int c = 0; c < BN / CW; ++c) {
                         float v[CW];
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) v[i] = 0.0f;
-                        for (int s = 0; s < it.nseg; ++s) {
-                            const float* src = base + static_cast<int64_t>(s) * (kTcBM * BN);
-#pragma unroll
-                            for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
-                        }
+                        // the swapped epilogue needs more registers: fewer pieces in flight
+                        sum_pieces<CW, SWAP ? (CW <= 16 ? 4 : 1) : 2>(v, base, it.nseg, kTcBM * BN, c * CW,
+                                                                   row);
                         apply_ab<SWAP, CW>(args, v, p, q0 + c * CW);
                         if constexpr (!SWAP) {
                             if (tma_out) {
@@ -1006,18 +1036,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
+                    // pieces of this CTA's rows: slot (tile, piece, CTA), pieces 2 slots apart
+                    const float* base =
+                        args.ws + (static_cast<int64_t>(it.slot) * args.max_seg * 2 + rank) * (kTcBM * BN);
 #pragma unroll 1
                     for (int c = 0; c < BN / CW; ++c) {
                         float v[CW];
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) v[i] = 0.0f;
-                        for (int sg = 0; sg < it.nseg; ++sg) {
-                            const float* src =
-                                args.ws + ((static_cast<int64_t>(it.slot) * args.max_seg + sg) * 2 + rank) *
-                                              (kTcBM * BN);
-#pragma unroll
-                            for (int i = 0; i < CW; ++i) v[i] += __ldcg(src + (c * CW + i) * kTcBM + row);
-                        }
+                        sum_pieces<CW, 2>(v, base, it.nseg, 2 * kTcBM * BN, c * CW, row);
                         apply_ab<false, CW>(args, v, p, q0 + c * CW);
                         if (args.tma_store)
                             stage_and_store(stg, &map_c, v, lane, q0 + c * CW, row0 + quarter * 32,
