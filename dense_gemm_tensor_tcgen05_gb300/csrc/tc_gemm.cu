@@ -41,12 +41,13 @@
 //
 // Back-to-back launches.  Both kernels are launched with programmatic stream
 // serialization: a launch may start while the previous kernel on the stream
-// is still finishing, runs its prologue (barrier set-up, tensor-memory
-// allocation, tensor-map prefetch) on the SMs that kernel has left, and
-// waits (griddepcontrol.wait) for it to complete before its first global
-// memory access.  A stream of GEMMs then hides most of each launch's
-// start-up; the order of every read and write of global memory is the same
-// as with plain launches.
+// is still finishing.  It runs its prologue (barrier set-up, tensor-memory
+// allocation, tensor-map prefetch) on the SMs that kernel has left, and the
+// producer plans its first tile from the kernel parameters.  Only then does
+// each role that touches global memory wait (griddepcontrol.wait) for the
+// previous kernel to complete.  A stream of GEMMs then hides most of each
+// launch's start-up; the order of every read and write of global memory is
+// the same as with plain launches.
 //
 // Waits.  Every mbarrier wait gives up after kWaitLimitNs, sets a bit in the
 // device error word and makes the whole CTA leave its loops; before exiting,
@@ -536,11 +537,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // Everything above touches only this CTA's shared and tensor memory, so
-    // it may overlap the previous kernel on the stream; every global access
-    // below comes after that kernel has finished.
+    // Everything above touches only this CTA's shared and tensor memory and
+    // the kernel parameters, so it may overlap the previous kernel on the
+    // stream.  Each role that touches global memory waits for that kernel
+    // (grid_dep_wait) before its first access: the producer before its first
+    // copy, the epilogue warps before their first access to C or the
+    // workspace.  The MMA thread touches none.
     grid_dep_launch_dependents();
-    grid_dep_wait();
     const WaitCtx wctx{abort_flag};
 
     if (warp == 0) {
@@ -550,6 +553,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;   // per-stage: armed at least once / parity
             bool ok = true;
+            bool dep_ready = false;
             WorkIter wi(args, blockIdx.x, gridDim.x);
             WorkItem it;
             while (ok && wi.next(args, it)) {
@@ -560,6 +564,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, wctx, kErrProducer)) {
                         ok = false;
                         break;
+                    }
+                    if (!dep_ready) {   // the first tile is planned; now the inputs may be read
+                        grid_dep_wait();
+                        dep_ready = true;
                     }
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, T::kStageBytes);
@@ -629,6 +637,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
         __syncwarp();
     } else {
         // ------------------------------ epilogue ----------------------------------
+        grid_dep_wait();
         const int quarter = warp & 3;                 // tensor-memory lanes 32*quarter ..
         const int row = quarter * 32 + lane;          // lane within the 128-row tile
         StoreStage stg{store_base + static_cast<uint32_t>(warp - 2) * 8192u, 0};
@@ -860,11 +869,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     cluster_sync();   // both CTAs' barriers exist and tensor memory is allocated
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // Everything above touches only this CTA's shared and tensor memory, so
-    // it may overlap the previous kernel on the stream; every global access
-    // below comes after that kernel has finished.
+    // Everything above touches only this CTA's shared and tensor memory and
+    // the kernel parameters, so it may overlap the previous kernel on the
+    // stream.  Each role that touches global memory waits for that kernel
+    // (grid_dep_wait) before its first access: the producer before its first
+    // copy, the epilogue warps before their first access to C or the
+    // workspace.  The MMA thread touches none.
     grid_dep_launch_dependents();
-    grid_dep_wait();
     const PairWaitCtx wctx{abort_flag,
                            mapa_shared(smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u)};
     const int cid = static_cast<int>(cluster_id_x());
@@ -877,6 +888,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;
             bool ok = true;
+            bool dep_ready = false;
             WorkIter wi(args, cid, ncl);
             WorkItem it;
             while (ok && wi.next(args, it)) {
@@ -888,6 +900,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                     if (!pair_wait_phase<false>(empty_bar(stage), phase ^ 1u, wctx, kErrProducer)) {
                         ok = false;
                         break;
+                    }
+                    if (!dep_ready) {   // the first tile is planned; now the inputs may be read
+                        grid_dep_wait();
+                        dep_ready = true;
                     }
                     if (leader) {
                         // both CTAs' bytes complete on this barrier
@@ -969,6 +985,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         __syncwarp();
     } else {
         // ------------------------------ epilogue (both CTAs) ----------------------
+        grid_dep_wait();
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         StoreStage stg{store_base + static_cast<uint32_t>(warp - 2) * 8192u, 0};
