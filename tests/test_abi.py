@@ -107,3 +107,22 @@ def test_transposed_leading_dimensions_checked_on_host(L):
     assert L.gemm_ex(P, 2 * P, 3 * P, 4, 4, 6, 6, 4, 4, ctypes.byref(o), None) == 1
     o.trans_b = 2
     assert L.gemm_ex(P, 2 * P, 3 * P, 4, 4, 4, 4, 4, 4, ctypes.byref(o), None) == 1
+
+
+def test_host_entry_checks_transposed_storage_on_host(L):
+    # gemm_ex_host takes the same transposed layouts as gemm_ex; the leading
+    # dimensions are those of the host arrays and are checked before any
+    # device work (host pointers here are never dereferenced)
+    o = g.GemmOptions()
+    o.dtype, o.swap_ab, o.trans_a = 1, -1, 1
+    assert L.gemm_ex_host(P, 2 * P, 3 * P, 8, 4, 4, 4, 4, 4, ctypes.byref(o), None) == 1   # lda < M
+    o.trans_a, o.trans_b = 0, 1
+    assert L.gemm_ex_host(P, 2 * P, 3 * P, 4, 4, 6, 6, 4, 4, ctypes.byref(o), None) == 1   # ldb < K
+    o.trans_b = 2
+    assert L.gemm_ex_host(P, 2 * P, 3 * P, 4, 4, 4, 4, 4, 4, ctypes.byref(o), None) == 1
+    o.trans_b, o.c_dtype = 0, 3
+    assert L.gemm_ex_host(P, 2 * P, 3 * P, 4, 4, 4, 4, 4, 4, ctypes.byref(o), None) == 1   # bad C type
+    # valid arguments get past the checks; without a GPU the call then stops
+    # at the device query, which is not an argument error
+    o.c_dtype, o.trans_a, o.trans_b = 0, 1, 1
+    assert L.gemm_ex_host(P, 2 * P, 3 * P, 4, 4, 6, 4, 6, 4, ctypes.byref(o), None) != 1
