@@ -23,8 +23,9 @@ import threading
 __all__ = [
     "GemmError", "lib", "library_path", "gemm_f16f32", "gemm_bf16f32", "sgemm_f32", "gemm_ex",
     "gemm_ex_noalloc", "gemm_ex_host", "gemm_plan_describe", "gemm_device_error",
-    "gemm_watchdog_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt", "gemm_e5m2f32_bt",
-    "gemm_release_workspace", "gemm_version", "gemm_launch_count", "matmul", "gemm", "plan",
+    "gemm_watchdog_selftest", "gemm_ex_stall_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt",
+    "gemm_e5m2f32_bt", "gemm_release_workspace", "gemm_version", "gemm_launch_count",
+    "gemm_alloc_count", "matmul", "gemm", "plan",
     "GemmOptions", "STATUS", "EXPORTED_SYMBOLS", "C_DTYPE",
 ]
 
@@ -48,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "gemm_device_error", "gemm_release_workspace", "gemm_status_string",
     "gemm_last_cuda_error", "gemm_version", "gemm_launch_count", "gemm_ex_noalloc",
     "gemm_ex_host", "gemm_watchdog_selftest", "gemm_tf32f32_bt", "gemm_e4m3f32_bt",
-    "gemm_e5m2f32_bt",
+    "gemm_e5m2f32_bt", "gemm_ex_stall_selftest", "gemm_alloc_count",
 )
 
 
@@ -110,6 +111,10 @@ def lib() -> ctypes.CDLL:
             L.gemm_device_error.restype = ctypes.c_int
             L.gemm_watchdog_selftest.argtypes = [ctypes.c_int32, vp]
             L.gemm_watchdog_selftest.restype = ctypes.c_int
+            L.gemm_ex_stall_selftest.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                                 ctypes.POINTER(GemmOptions), ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_int32, vp]
+            L.gemm_ex_stall_selftest.restype = ctypes.c_int
             L.gemm_release_workspace.argtypes = []
             L.gemm_release_workspace.restype = ctypes.c_int
             L.gemm_status_string.argtypes = [ctypes.c_int]
@@ -120,6 +125,8 @@ def lib() -> ctypes.CDLL:
             L.gemm_version.restype = ctypes.c_int32
             L.gemm_launch_count.argtypes = []
             L.gemm_launch_count.restype = ctypes.c_int64
+            L.gemm_alloc_count.argtypes = []
+            L.gemm_alloc_count.restype = ctypes.c_int64
             _lib = L
     return _lib
 
@@ -223,6 +230,17 @@ def gemm_watchdog_selftest(limit_ms: int = 20, stream: int = 0) -> None:
     _check(lib().gemm_watchdog_selftest(limit_ms, stream or None))
 
 
+def gemm_ex_stall_selftest(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                           ldc: int, dtype: int, limit_ms: int, stall_cta: int, stall_fill: int,
+                           stream: int = 0, **opts) -> None:
+    """Run a tensor-core plan whose pipeline waits give up after limit_ms,
+    with one CTA's producer withholding one stage (see include/gb300gemm.h).
+    The timeout is then reported by gemm_device_error()."""
+    o = _options(dtype, **opts)
+    _check(lib().gemm_ex_stall_selftest(A, B, C, M, N, K, lda, ldb, ldc, ctypes.byref(o),
+                                        limit_ms, stall_cta, stall_fill, stream or None))
+
+
 def gemm_release_workspace() -> None:
     _check(lib().gemm_release_workspace())
 
@@ -233,6 +251,10 @@ def gemm_version() -> int:
 
 def gemm_launch_count() -> int:
     return int(lib().gemm_launch_count())
+
+
+def gemm_alloc_count() -> int:
+    return int(lib().gemm_alloc_count())
 
 
 # ---- torch convenience -------------------------------------------------------

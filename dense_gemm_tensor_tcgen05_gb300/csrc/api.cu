@@ -6,6 +6,7 @@
 // the page passages they follow.
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdio>
 #include <cstring>
@@ -23,6 +24,7 @@ namespace {
 
 thread_local char t_last_error[256] = "";
 thread_local int64_t t_launches = 0;
+std::atomic<int64_t> g_allocs{0};   // device allocations made by the library (all threads)
 
 void note_cuda_error(cudaError_t e, const char* where) {
     snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
@@ -118,6 +120,50 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// ---- the current CUDA context ---------------------------------------------------
+//
+// Device pointers and stream handles the library caches belong to the CUDA
+// context that was current when they were made.  cudaDeviceReset destroys
+// the device's primary context (and every allocation in it); the next call
+// then runs in a new context, where a cached pointer would be invalid.  So
+// caches record the context's unique id (cuCtxGetId) and are dropped, not
+// freed, when it changes.
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id (+1) of the context current on this thread, making the device's
+// primary context current first if none is; 0 if it cannot be told.
+uint64_t current_ctx_id(int dev) {
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS) return 0;
+    if (!c) {   // cudaSetDevice initialises the primary context and makes it current
+        if (cudaSetDevice(dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    }
+    unsigned long long id = 0;
+    if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return static_cast<uint64_t>(id) + 1;
+}
+
 // ---- split-K workspace, one per (device, stream) --------------------------------
 
 struct Workspace {
@@ -125,15 +171,28 @@ struct Workspace {
     size_t ws_floats = 0;
     uint32_t* counters = nullptr;
     size_t n_counters = 0;
+    uint64_t ctx = 0;     // context the buffers belong to
+    uint64_t epoch = 0;   // g_ws_epoch[dev] when the counters were last known to be zero
 };
 
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// Per device: bumped each time gemm_device_error finds that a kernel gave up
+// a wait.  A kernel that aborts may leave tile counters part-way, so every
+// workspace of the device clears its counters before its next use.
+std::map<int, uint64_t> g_ws_epoch;
 
 gemm_status_t get_workspace(int dev, cudaStream_t stream, size_t floats, size_t counters,
                             float** ws, uint32_t** cnt) {
+    const uint64_t ctx = current_ctx_id(dev);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace& w = g_ws[{dev, stream}];
+    if (ctx && w.ctx != ctx) {
+        // made in a context that no longer exists (or none yet): forget it
+        w = Workspace{};
+        w.ctx = ctx;
+    }
+    const uint64_t epoch = g_ws_epoch[dev];
     if (w.ws_floats < floats) {
         if (w.ws) {
             cudaStreamSynchronize(stream);   // the old buffer may still be in use on this stream
@@ -147,6 +206,7 @@ gemm_status_t get_workspace(int dev, cudaStream_t stream, size_t floats, size_t 
             w.ws = nullptr;
             return GEMM_ERR_OUT_OF_MEMORY;
         }
+        ++g_allocs;
         w.ws_floats = floats;
     }
     if (w.n_counters < counters) {
@@ -162,13 +222,19 @@ gemm_status_t get_workspace(int dev, cudaStream_t stream, size_t floats, size_t 
             w.counters = nullptr;
             return GEMM_ERR_OUT_OF_MEMORY;
         }
-        // Counters start at zero and every launch leaves them at zero.
-        e = cudaMemsetAsync(w.counters, 0, counters * sizeof(uint32_t), stream);
+        ++g_allocs;
+        w.n_counters = counters;
+        w.epoch = epoch + 1;   // cleared below
+    }
+    // Counters start at zero and every completed launch leaves them at zero;
+    // after a reported timeout (or when new) they are cleared on the stream.
+    if (w.epoch != epoch) {
+        cudaError_t e = cudaMemsetAsync(w.counters, 0, w.n_counters * sizeof(uint32_t), stream);
         if (e != cudaSuccess) {
             note_cuda_error(e, "cudaMemsetAsync(split-K counters)");
             return GEMM_ERR_CUDA;
         }
-        w.n_counters = counters;
+        w.epoch = epoch;
     }
     *ws = w.ws;
     *cnt = w.counters;
@@ -559,9 +625,15 @@ gemm_status_t launch_status(cudaError_t e, const char* what) {
     return GEMM_ERR_LAUNCH;
 }
 
+// A self-test of the tensor-core kernels' bounded waits (gemm_ex_stall_selftest).
+struct StallTest {
+    uint64_t limit_ns;
+    int cta, fill;
+};
+
 gemm_status_t run(int dtype, const void* A, const void* B, void* C, int64_t M, int64_t N,
                   int64_t K, int64_t lda, int64_t ldb, int64_t ldc, const gemm_options_t& o,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const StallTest* stall = nullptr) {
     if (dtype < 0 || dtype > 5) return GEMM_ERR_INVALID_VALUE;
     const int esize = dtype_bytes(dtype);
     gemm_status_t st = check_args(A, B, C, M, N, K, lda, ldb, ldc, esize, o.trans_a, o.trans_b,
@@ -575,6 +647,20 @@ gemm_status_t run(int dtype, const void* A, const void* B, void* C, int64_t M, i
     Plan p;
     st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, o, info.sms, &p);
     if (st != GEMM_OK) return st;
+    if (stall) {
+        // only the tensor-core kernels have pipeline waits; the stalled CTA
+        // (pair kernel: cluster) must exist
+        const int units = p.tc.pair ? p.tc.grid / 2 : p.tc.grid;
+        if (p.kind != Kind::Tc || stall->cta < 0 || stall->cta >= units || stall->fill < 0) {
+            snprintf(t_last_error, sizeof(t_last_error),
+                     "stall self-test needs a tensor-core plan, 0 <= stall_cta < %d, stall_fill >= 0",
+                     p.kind == Kind::Tc ? units : 0);
+            return GEMM_ERR_INVALID_VALUE;
+        }
+        p.tc.wait_limit_ns = stall->limit_ns;
+        p.tc.stall_cta = stall->cta;
+        p.tc.stall_fill = stall->fill + 1;
+    }
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;
         case Kind::ZeroFill:   // the empty sum: beta * C, or zeros
@@ -692,7 +778,13 @@ gemm_status_t gemm_plan_describe(int32_t dtype, const void* A, const void* B, co
 }
 
 gemm_status_t gemm_device_error(gemm_stream_t stream) {
-    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        note_cuda_error(e, "cudaGetDevice");
+        return GEMM_ERR_CUDA;
+    }
+    e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         note_cuda_error(e, "cudaStreamSynchronize");
         return GEMM_ERR_CUDA;
@@ -714,6 +806,12 @@ gemm_status_t gemm_device_error(gemm_stream_t stream) {
         if (e != cudaSuccess) {
             note_cuda_error(e, "cudaMemset(error word)");
             return GEMM_ERR_CUDA;
+        }
+        {
+            // a kernel that gave up may have left split-K tile counters part-way:
+            // every workspace of this device clears them before its next use
+            std::lock_guard<std::mutex> lk(g_ws_mu);
+            ++g_ws_epoch[dev];
         }
         snprintf(t_last_error, sizeof(t_last_error), "device pipeline wait gave up (bits 0x%x)", v);
         return GEMM_ERR_DEVICE_TIMEOUT;
@@ -744,11 +842,14 @@ gemm_status_t gemm_release_workspace(void) {
         note_cuda_error(e, "cudaDeviceSynchronize");
         return GEMM_ERR_CUDA;
     }
+    const uint64_t ctx = current_ctx_id(dev);
     std::lock_guard<std::mutex> lk(g_ws_mu);
     for (auto it = g_ws.begin(); it != g_ws.end();) {
         if (it->first.first == dev) {
-            cudaFree(it->second.ws);
-            cudaFree(it->second.counters);
+            if (!ctx || it->second.ctx == ctx) {   // else its context (and memory) is gone
+                cudaFree(it->second.ws);
+                cudaFree(it->second.counters);
+            }
             it = g_ws.erase(it);
         } else {
             ++it;
@@ -773,9 +874,21 @@ const char* gemm_status_string(gemm_status_t s) {
 
 const char* gemm_last_cuda_error(void) { return t_last_error; }
 
-int32_t gemm_version(void) { return 100; }
+int32_t gemm_version(void) { return 200; }
 
 int64_t gemm_launch_count(void) { return t_launches; }
+
+int64_t gemm_alloc_count(void) { return g_allocs.load(); }
+
+gemm_status_t gemm_ex_stall_selftest(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                     const gemm_options_t* options, int32_t limit_ms,
+                                     int32_t stall_cta, int32_t stall_fill, gemm_stream_t stream) {
+    if (!options || limit_ms < 1 || limit_ms > 2000) return GEMM_ERR_INVALID_VALUE;
+    const StallTest t{static_cast<uint64_t>(limit_ms) * 1000000ull, stall_cta, stall_fill};
+    return run(options->dtype, A, B, C, M, N, K, lda, ldb, ldc, *options,
+               reinterpret_cast<cudaStream_t>(stream), &t);
+}
 
 }  // extern "C"
 
@@ -801,13 +914,17 @@ constexpr int kNoallocMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoallocMaxDevices];   // device address per device, or null
+void* g_noalloc_addr[kNoallocMaxDevices];       // device address per device, or null
+uint64_t g_noalloc_ctx[kNoallocMaxDevices];     // context the address belongs to
 
-// Device address of the scratch array on `dev` (which must be current).
+// Device address of the scratch array on `dev` (which must be current).  It
+// is looked up once per device and context (a cudaDeviceReset makes a new
+// context, in which the array has a new address).
 gemm_status_t noalloc_scratch(int dev, unsigned char** out) {
     if (dev < 0 || dev >= kNoallocMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    const uint64_t ctx = current_ctx_id(dev);
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    if (!g_noalloc_addr[dev] || (ctx && g_noalloc_ctx[dev] != ctx)) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) {
@@ -815,6 +932,7 @@ gemm_status_t noalloc_scratch(int dev, unsigned char** out) {
             return GEMM_ERR_CUDA;
         }
         g_noalloc_addr[dev] = p;
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = static_cast<unsigned char*>(g_noalloc_addr[dev]);
     return GEMM_OK;
@@ -936,6 +1054,7 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, void* C, 
 namespace {
 
 struct HostPipe {
+    uint64_t ctx = 0;   // context the streams, events and buffers belong to
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t e_start = nullptr, e_a = nullptr, e_b = nullptr, e_blk = nullptr;
     cudaEvent_t e_rowcomp[2] = {}, e_rowout[2] = {};
@@ -963,6 +1082,7 @@ gemm_status_t grow(void** p, size_t* have, size_t want, const char* what) {
         *p = nullptr;
         return GEMM_ERR_OUT_OF_MEMORY;
     }
+    ++g_allocs;
     *have = want;
     return GEMM_OK;
 }
@@ -970,6 +1090,11 @@ gemm_status_t grow(void** p, size_t* have, size_t want, const char* what) {
 gemm_status_t host_pipe(int dev, cudaStream_t stream, size_t b_bytes, size_t a_bytes,
                         size_t c_bytes, HostPipe** out) {
     HostPipe& h = g_hp[{dev, stream}];
+    const uint64_t ctx = current_ctx_id(dev);
+    if (ctx && h.ctx != ctx) {   // made in a context that no longer exists (or none yet)
+        h = HostPipe{};
+        h.ctx = ctx;
+    }
     cudaError_t e = cudaSuccess;
     if (!h.s_in) {
         cudaEvent_t* evs[] = {&h.e_start, &h.e_a, &h.e_b, &h.e_blk, &h.e_rowcomp[0],

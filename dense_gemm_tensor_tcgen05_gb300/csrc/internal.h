@@ -37,6 +37,11 @@ struct TcLaunch {
     int grid;       // CTAs (persistent); <= units
     float* ws;          // split-K partial tiles (splits * tiles * 128 * bn floats), or null
     uint32_t* counters; // split-K arrival counters (tiles * 4), zero between launches, or null
+    // Self-test of the kernels' own bounded waits (gemm_ex_stall_selftest);
+    // all zero for a normal launch.
+    uint64_t wait_limit_ns;  // 0: the kernels' default limit
+    int stall_cta;           // CTA (pair kernel: cluster) whose producer withholds one stage
+    int stall_fill;          // 1 + index of the stage fill it withholds; 0: none
 };
 
 // Tile geometry helpers used by the planner and the launcher.

@@ -60,7 +60,10 @@
 // Waits.  Every mbarrier wait gives up after kWaitLimitNs, sets a bit in the
 // device error word and makes the whole CTA leave its loops; before exiting,
 // the producer waits (bounded) for its own TMA copies and the MMA thread for
-// its own MMAs, and tensor memory is freed on every path.
+// its own MMAs, and tensor memory is freed on every path.  A self-test launch
+// (TcArgs::stall_cta >= 0) shortens the limit and has one CTA's (or pair's)
+// producer withhold the copies of one stage, so that this path runs: the
+// MMA thread's wait for that stage runs out and the CTA aborts.
 
 #include <algorithm>
 #include <cstdio>
@@ -110,6 +113,9 @@ struct TcArgs {
     uint32_t idesc;
     float* ws;
     uint32_t* counters;
+    uint64_t wait_limit_ns;     // limit of every pipeline wait (kWaitLimitNs unless a self-test)
+    int32_t stall_cta;          // self-test: this CTA (pair: cluster) withholds one stage; -1 none
+    int32_t stall_fill;         // self-test: index of the stage fill it withholds
 };
 
 template <int BN, bool SWAP>
@@ -134,18 +140,19 @@ struct TcTraits {
 
 struct WaitCtx {
     volatile uint32_t* abort_flag;
+    uint64_t limit_ns;   // give up after this long
 };
 
 // Bounded wait: true when the phase of the given parity completed; false when
 // the CTA is aborting (this wait gave up, or another role did).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                           uint32_t err_bit, uint64_t limit_ns = kWaitLimitNs) {
+                                           uint32_t err_bit) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
+        if (globaltimer_ns() - t0 > w.limit_ns) {
             *w.abort_flag = 1;
             atomicOr(&g_tc_error, err_bit);
             return false;
@@ -552,7 +559,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
     // copy, the epilogue warps before their first access to C or the
     // workspace.  The MMA thread touches none.
     grid_dep_launch_dependents();
-    const WaitCtx wctx{abort_flag};
+    const WaitCtx wctx{abort_flag, args.wait_limit_ns};
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
@@ -565,6 +572,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
             WorkIter wi(args, blockIdx.x, gridDim.x);
             WorkItem it;
             int items = 0;
+            // self-test only: the fill index whose copies this CTA withholds
+            const int stall = (static_cast<int>(blockIdx.x) == args.stall_cta) ? args.stall_fill : -1;
+            int fills = 0;
             while (ok && wi.next(args, it)) {
                 int pb, qb;
                 tile_coords(args, it.tile, pb, qb);
@@ -581,15 +591,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_p, const __grid_constant_
                         grid_dep_wait();
                         dep_ready = true;
                     }
-                    const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, T::kStageBytes);
-                    armed |= 1u << stage;
-                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    const uint32_t sp = smem_base + stage * T::kStageBytes;
-                    const uint32_t sq = sp + T::kPBytes;
-                    const int k0 = kb * kind_k_elems(KIND);
-                    load_operand<kTcBM>(sp, &map_p, fb, args.p_kmajor, p0, k0);
-                    load_operand<BN>(sq, &map_q, fb, args.q_kmajor, q0, k0);
+                    if (fills++ != stall) {
+                        const uint32_t fb = full_bar(stage);
+                        mbar_arrive_expect_tx(fb, T::kStageBytes);
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        const uint32_t sp = smem_base + stage * T::kStageBytes;
+                        const uint32_t sq = sp + T::kPBytes;
+                        const int k0 = kb * kind_k_elems(KIND);
+                        load_operand<kTcBM>(sp, &map_p, fb, args.p_kmajor, p0, k0);
+                        load_operand<BN>(sq, &map_q, fb, args.q_kmajor, q0, k0);
+                    }
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -801,6 +813,7 @@ struct PairTraits {
 struct PairWaitCtx {
     volatile uint32_t* abort_flag;   // this CTA's flag (the peer may set it remotely)
     uint32_t peer_abort;             // shared::cluster address of the peer's flag
+    uint64_t limit_ns;               // give up after this long
 };
 
 __device__ __forceinline__ void pair_raise_abort(const PairWaitCtx& w) {
@@ -819,7 +832,7 @@ __device__ __forceinline__ bool pair_wait_phase(uint32_t bar, uint32_t parity,
     while (true) {
         if (test()) return true;
         if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > w.limit_ns) {
             atomicOr(&g_tc_error, err_bit);
             pair_raise_abort(w);
             return false;
@@ -889,7 +902,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     // workspace.  The MMA thread touches none.
     grid_dep_launch_dependents();
     const PairWaitCtx wctx{abort_flag,
-                           mapa_shared(smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u)};
+                           mapa_shared(smem_u32(const_cast<uint32_t*>(abort_flag)), rank ^ 1u),
+                           args.wait_limit_ns};
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(cluster_count_x());
 
@@ -904,6 +918,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             WorkIter wi(args, cid, ncl);
             WorkItem it;
             int items = 0;
+            // self-test only: both CTAs of the stalled pair withhold the same
+            // fill (the even CTA does not arm it, the odd CTA copies nothing
+            // into it), so no copy is left in flight for that stage
+            const int stall = (cid == args.stall_cta) ? args.stall_fill : -1;
+            int fills = 0;
             while (ok && wi.next(args, it)) {
                 int pb, qb;
                 tile_coords(args, it.tile, pb, qb);
@@ -921,23 +940,25 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
                         grid_dep_wait();
                         dep_ready = true;
                     }
-                    if (leader) {
-                        // both CTAs' bytes complete on this barrier
-                        mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
-                        armed |= 1u << stage;
-                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    }
-                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
-                    const uint32_t sa = smem_base + stage * T::kStageBytes;
-                    const uint32_t sb = sa + T::kABytes;
-                    // atoms past K are fetched too: the copy fills them with zeros
+                    if (fills++ != stall) {
+                        if (leader) {
+                            // both CTAs' bytes complete on this barrier
+                            mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
+                            armed |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                        const uint32_t sa = smem_base + stage * T::kStageBytes;
+                        const uint32_t sb = sa + T::kABytes;
+                        // atoms past K are fetched too: the copy fills them with zeros
 #pragma unroll
-                    for (int j = 0; j < T::kAtoms; ++j) {
-                        const int k0 = (ks * T::kAtoms + j) * kind_k_elems(KIND);
-                        load_operand_pair<kTcBM>(sa + j * T::kAAtomBytes, &map_a, fb, args.p_kmajor,
-                                                 m0, k0);
-                        load_operand_pair<BN / 2>(sb + j * T::kBAtomBytes, &map_b, fb, args.q_kmajor,
-                                                  n0, k0);
+                        for (int j = 0; j < T::kAtoms; ++j) {
+                            const int k0 = (ks * T::kAtoms + j) * kind_k_elems(KIND);
+                            load_operand_pair<kTcBM>(sa + j * T::kAAtomBytes, &map_a, fb,
+                                                     args.p_kmajor, m0, k0);
+                            load_operand_pair<BN / 2>(sb + j * T::kBAtomBytes, &map_b, fb,
+                                                      args.q_kmajor, n0, k0);
+                        }
                     }
                     if (++stage == S) {
                         stage = 0;
@@ -1135,8 +1156,8 @@ __global__ void watchdog_selftest_kernel(uint64_t limit_ns) {
         mbar_init(smem_u32(&bar), 1);
         abort_flag = 0;
         fence_barrier_init();
-        const WaitCtx w{&abort_flag};
-        wait_phase(smem_u32(&bar), 0, w, kErrSelfTest, limit_ns);
+        const WaitCtx w{&abort_flag, limit_ns};
+        wait_phase(smem_u32(&bar), 0, w, kErrSelfTest);
     }
 }
 
@@ -1383,6 +1404,9 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.ab = L.ab;
     a.alpha = L.alpha;
     a.beta = L.beta;
+    a.wait_limit_ns = L.wait_limit_ns ? L.wait_limit_ns : kWaitLimitNs;
+    a.stall_cta = L.stall_fill > 0 ? L.stall_cta : -1;
+    a.stall_fill = L.stall_fill - 1;
 
     const CUtensorMap& mp = L.swap ? map_b : map_a;
     const CUtensorMap& mq = L.swap ? map_a : map_b;

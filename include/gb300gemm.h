@@ -34,7 +34,9 @@
  * them.  C must not overlap A or B.  The library owns a small per-device,
  * per-stream split-K workspace (partial tiles + tile counters) that it
  * allocates on first use and grows as needed; gemm_release_workspace() frees
- * it.
+ * it.  Its caches remember the CUDA context they were made in: after a
+ * cudaDeviceReset the next call starts afresh instead of using pointers of
+ * the destroyed context.
  *
  * Streams: every call enqueues its kernels on `stream` (NULL = the legacy
  * default stream) and returns without synchronising.  A fault in a kernel
@@ -251,7 +253,10 @@ gemm_status_t gemm_plan_describe(int32_t dtype, const void *A, const void *B, co
  * current device's error flag.  Returns GEMM_ERR_DEVICE_TIMEOUT if any
  * kernel since the last call gave up a pipeline wait (it then wrote no
  * trustworthy output), GEMM_ERR_CUDA if the synchronisation failed, else
- * GEMM_OK.
+ * GEMM_OK.  A kernel that gives up may leave split-K tile counters part-way;
+ * on GEMM_ERR_DEVICE_TIMEOUT every split-K workspace of the device is
+ * therefore marked, and each clears its counters (an asynchronous memset on
+ * its stream) before it is next used, so later calls are correct again.
  */
 gemm_status_t gemm_device_error(gemm_stream_t stream);
 
@@ -266,6 +271,30 @@ gemm_status_t gemm_device_error(gemm_stream_t stream);
  * counterpart.)
  */
 gemm_status_t gemm_watchdog_selftest(int32_t limit_ms, gemm_stream_t stream);
+
+/*
+ * gemm_ex_stall_selftest -- checks the GEMM kernels' own failure path.  Runs
+ * the tensor-core plan gemm_ex would run for these arguments (other plans:
+ * GEMM_ERR_INVALID_VALUE) with two changes: every pipeline wait gives up
+ * after limit_ms (1..2000) milliseconds, and the TMA producer of CTA
+ * `stall_cta` (for the CTA-pair kernel: of both CTAs of cluster `stall_cta`)
+ * withholds the copies of its pipeline stage number `stall_fill` (0 = the
+ * first stage it fills).  The MMA thread's wait for that stage then runs
+ * out; the CTA (pair) records GEMM_ERR_DEVICE_TIMEOUT in the device error
+ * word, leaves its loops, waits (bounded) for its copies and MMAs in flight,
+ * frees its tensor memory and exits, while the other CTAs finish normally.
+ * Nothing faults, traps or hangs; the context stays usable.  C is then
+ * unspecified (the stalled CTA's tiles are missing).  stall_cta must be below
+ * the plan's CTA (cluster) count; a CTA with fewer than stall_fill + 1 stage
+ * fills runs normally.  (A testing aid of this library; the pages have no
+ * counterpart.)
+ */
+gemm_status_t gemm_ex_stall_selftest(const void *A, const void *B, void *C,
+                                     int64_t M, int64_t N, int64_t K,
+                                     int64_t lda, int64_t ldb, int64_t ldc,
+                                     const gemm_options_t *options, int32_t limit_ms,
+                                     int32_t stall_cta, int32_t stall_fill,
+                                     gemm_stream_t stream);
 
 /* gemm_release_workspace -- frees the split-K workspaces of the current
  * device after synchronising the device.  Later calls allocate again. */
@@ -316,17 +345,25 @@ gemm_status_t gemm_ex_host(const void *A, const void *B, void *C,
  * entry point never calls cudaMalloc, cudaFree or any other allocating
  * routine.  The caller still passes A, B and C.
  *
- * Scratch: the split-K tensor-core kernel keeps its partial tiles and arrival
- * counters in one static device array of GEMM_NOALLOC_SCRATCH_BYTES (8 MiB:
- * the first 64 KiB hold counters for up to 4096 tiles, the rest holds partial
- * tiles).  Every GPU that loads the library holds this array until the
- * process exits.  A plan whose scratch does not fit returns
- * GEMM_ERR_INVALID_VALUE, and gemm_last_cuda_error() says how much it needed.
- * Plans without split-K use no scratch at all.
+ * Scratch: every plan that splits tiles along K keeps its partial tiles and
+ * arrival counters in one static device array of GEMM_NOALLOC_SCRATCH_BYTES
+ * (8 MiB: the first 64 KiB hold counters for up to 4096 tiles, the rest
+ * holds partial tiles) -- the split-K and stream-K plans of the tensor-core
+ * kernels (one CTA or CTA pairs) and the split-K plans of the FP32 SGEMM.
+ * Every GPU that loads the library holds this array until the process exits.
+ * A plan whose scratch does not fit returns GEMM_ERR_INVALID_VALUE, and
+ * gemm_last_cuda_error() says how much it needed.  Plans that do not split
+ * tiles use no scratch at all.  The results are bit-identical to gemm_ex's
+ * for the same plan.
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.
+ * before any stream capture.  Under CUDA's lazy module loading (the default)
+ * the library's device code, and with it this array, is placed in device
+ * memory when it is first used -- by the first call of each kind.  A caller
+ * that must not allocate later should make one call of each plan kind it
+ * will use at start-up, before it hands the remaining memory to its pool
+ * (or run with CUDA_MODULE_LOADING=EAGER).
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents; each call clears the counters it needs (an asynchronous
@@ -356,6 +393,11 @@ int32_t gemm_version(void);
 /* Number of kernel launches this host thread has enqueued through the library
  * since it loaded (monotonic counter, for accounting in benchmarks). */
 int64_t gemm_launch_count(void);
+
+/* Number of device allocations (cudaMalloc) the library has made since it
+ * loaded, over all threads and devices: split-K workspaces and gemm_ex_host's
+ * staging buffers (monotonic counter; gemm_ex_noalloc never adds to it). */
+int64_t gemm_alloc_count(void);
 
 #ifdef __cplusplus
 }

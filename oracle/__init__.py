@@ -42,7 +42,8 @@ import numpy as np
 
 __all__ = [
     "F16", "BF16", "F32", "build", "lib", "decode", "gemm", "gemm_rows", "gemm_general", "gemm_op",
-    "general_bounds", "tf32_bound", "E4M3", "E5M2", "encode16", "round16", "half_ulp16",
+    "general_bounds", "tf32_bound", "tf32_cut", "E4M3", "E5M2", "encode16", "round16",
+    "half_ulp16",
     "gemm_entries", "compare", "Comparison", "ABS_COEF", "REL_FROB",
 ]
 
@@ -279,6 +280,26 @@ def tf32_bound(abs_sums: np.ndarray) -> np.ndarray:
     magnitudes.  abs_sums[i, j] = sum_k |A[i][k]| |B[k][j]| (the oracle's
     product of the absolute values)."""
     return (2.0 ** -9 + 2.0 ** -20) * np.asarray(abs_sums, dtype=np.float64)
+
+
+def tf32_cut(x, mode: str) -> np.ndarray:
+    """FP32 values cut to TF32 (a float32 array of the same shape).
+
+    TF32 keeps FP32's sign and 8-bit exponent and 10 of its 23 fraction bits.
+    The pages only say that the TF32 mode changes results ("matmul_registers.cu",
+    the note on CUBLAS_COMPUTE_32F), not how the 13 low fraction bits go, so
+    both readings are offered: mode "trunc" drops them; mode "rne" rounds
+    them to nearest, ties to even (a carry may raise the exponent).  For
+    finite inputs only."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    if mode == "trunc":
+        out = u & 0xFFFFE000
+    elif mode == "rne":
+        keep_lsb = (u >> 13) & 1            # the lowest kept fraction bit
+        out = (u + 0xFFF + keep_lsb) & 0xFFFFE000
+    else:
+        raise ValueError("mode is 'trunc' or 'rne'")
+    return out.astype(np.uint32).view(np.float32)
 
 
 def general_bounds(K: int, max_abs_a: float, max_abs_b: float, alpha: float, beta: float,

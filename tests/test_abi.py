@@ -44,7 +44,7 @@ def test_status_strings_and_version(L):
     for code, name in g.STATUS.items():
         assert L.gemm_status_string(code).decode().startswith(name)
     assert L.gemm_status_string(99).decode() == "unknown gemm_status_t"
-    assert g.gemm_version() == 100
+    assert g.gemm_version() == 200
 
 
 # Argument errors are reported before any CUDA call, so these run without a GPU.
@@ -126,3 +126,20 @@ def test_host_entry_checks_transposed_storage_on_host(L):
     # at the device query, which is not an argument error
     o.c_dtype, o.trans_a, o.trans_b = 0, 1, 1
     assert L.gemm_ex_host(P, 2 * P, 3 * P, 4, 4, 6, 4, 6, 4, ctypes.byref(o), None) != 1
+
+
+def test_stall_selftest_checks_its_arguments_on_host(L):
+    # the wait limit is checked before anything else; options are required
+    o = g.GemmOptions()
+    o.dtype, o.swap_ab = 1, -1
+    args = (P, 2 * P, 3 * P, 256, 256, 256, 256, 256, 256)
+    assert L.gemm_ex_stall_selftest(*args, ctypes.byref(o), 0, 0, 0, None) == 1
+    assert L.gemm_ex_stall_selftest(*args, ctypes.byref(o), 2001, 0, 0, None) == 1
+    assert L.gemm_ex_stall_selftest(*args, None, 20, 0, 0, None) == 1
+    # a valid request gets past the checks and stops at the device query here
+    assert L.gemm_ex_stall_selftest(*args, ctypes.byref(o), 20, 0, 0, None) not in (0, 1)
+
+
+def test_alloc_count_starts_at_zero_without_a_gpu(L):
+    # nothing above allocated device memory (every call stopped on the host)
+    assert g.gemm_alloc_count() == 0

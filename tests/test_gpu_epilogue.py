@@ -44,6 +44,9 @@ def _check(dt, M, N, K, alpha, beta, opts, dist="uniform", ldc_pad=0, exact=Fals
     err = np.abs(C.astype(np.float64) - R)
     assert np.all(np.isfinite(C)), "non-finite output"
     assert err.max() <= bound, f"max err {err.max():.3e} > {bound:.3e}"
+    # the relative Frobenius half of the acceptance rule
+    rel = np.linalg.norm(C.astype(np.float64) - R) / np.linalg.norm(R)
+    assert rel <= oracle.REL_FROB, f"relative Frobenius error {rel:.3e}"
     if exact:
         assert np.array_equal(C, R.astype(np.float32))
 

@@ -4,7 +4,9 @@ latency-critical loops where a cudaMalloc/cudaFree, which can synchronise the
 device, is not acceptable).  Its split-K scratch lives in a fixed array inside
 the library, so here it is compared with gemm_ex, which allocates its
 workspace, on the same inputs and plans, twice in a row -- the second call
-reuses the array the first one left behind.
+reuses the array the first one left behind.  Both run the same plan, whose
+split-K sums are taken in a fixed order, so the results must be identical
+bit for bit; both are also checked against the oracle.
 
 Collected last on purpose (file name), so a run that stops at the first
 failure has run every other test first; it also passes alone in a fresh
@@ -71,28 +73,47 @@ def test_noalloc_matches_gemm_ex_twice(L, case):
     Ad, Bd = gu.to_device(A, dt), gu.to_device(B, dt)
     ref = _call(L, "gemm_ex", dt, Ad, Bd, M, N, K, opts)
     amax, bmax = inputs.bits_abs_max(A, dt), inputs.bits_abs_max(B, dt)
+    R = oracle.gemm(dt, A, B)
+    assert oracle.compare(ref, R, K, amax, bmax).ok
     for _ in range(2):
         got = _call(L, "gemm_ex_noalloc", dt, Ad, Bd, M, N, K, opts)
-        cmp = oracle.compare(got, ref.astype(np.float64), K, amax, bmax)
+        assert np.array_equal(got, ref), "gemm_ex_noalloc differs from gemm_ex on the same plan"
+        cmp = oracle.compare(got, R, K, amax, bmax)
         assert cmp.ok, str(cmp)
 
 
-def test_noalloc_repeat_calls_take_no_device_memory(L):
+def test_noalloc_small_integers_exact_twice(L):
+    # exact inputs: every summation order gives the oracle's value
+    dt, M, N, K, opts = CASES[1]
+    A, B = gu.make_inputs(dt, "small_int", M, N, K, 0)
+    Ad, Bd = gu.to_device(A, dt), gu.to_device(B, dt)
+    want = oracle.gemm(dt, A, B).astype(np.float32)
+    for _ in range(2):
+        assert np.array_equal(_call(L, "gemm_ex_noalloc", dt, Ad, Bd, M, N, K, opts), want)
+
+
+def test_noalloc_repeat_calls_allocate_nothing(L):
+    # The library counts every device allocation it makes (gemm_alloc_count);
+    # other processes or torch's caching allocator do not touch this count.
     import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
     dt, M, N, K, opts = CASES[0]
     A, B = gu.make_inputs(dt, "uniform", M, N, K, 78)
     Ad, Bd = gu.to_device(A, dt), gu.to_device(B, dt)
     C = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream().cuda_stream
+    fresh = torch.cuda.Stream()                   # a stream no call has used yet
     o = _opts(dt, **opts)
-    args = (Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, K, N, N, ctypes.byref(o), stream)
-    assert L.gemm_ex_noalloc(*args) == 0          # set-up happens on the first call
-    torch.cuda.synchronize()
-    free_before = torch.cuda.mem_get_info()[0]
+    args = (Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K, K, N, N, ctypes.byref(o))
+    before = g.gemm_alloc_count()
     for _ in range(3):
-        assert L.gemm_ex_noalloc(*args) == 0
+        assert L.gemm_ex_noalloc(*args, fresh.cuda_stream) == 0
     torch.cuda.synchronize()
-    assert torch.cuda.mem_get_info()[0] == free_before
+    assert g.gemm_alloc_count() == before
+    # the same split-K plan through gemm_ex on that stream allocates its
+    # workspace, so the counter does see allocations
+    assert L.gemm_ex(*args, fresh.cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert g.gemm_alloc_count() > before
 
 
 def test_noalloc_rejects_scratch_beyond_maximum(L):
