@@ -87,17 +87,18 @@ int pair_clusters() {
     return cache[dev];
 }
 
-// Resident SGEMM CTAs on the whole device for a tile shape (cached per device).
-int sgemm_slots(int bm, int bn, int sms) {
+// Resident SGEMM CTAs on the whole device for a tile shape and kernel form
+// (split or stream-K), cached per device.
+int sgemm_slots(int bm, int bn, int sms, bool stream_k = false) {
     static std::mutex mu;
-    static int cache[64][3];
+    static int cache[64][6];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const int idx = (bm == 128 && bn == 128) ? 0 : (bm == 128 ? 1 : 2);
+    const int idx = ((bm == 128 && bn == 128) ? 0 : (bm == 128 ? 1 : 2)) + (stream_k ? 3 : 0);
     std::lock_guard<std::mutex> lk(mu);
     if (!cache[dev][idx]) {
         int n = 0;
-        if (sgemm_blocks_per_sm(bm, bn, &n) != cudaSuccess) {
+        if (sgemm_blocks_per_sm(bm, bn, stream_k, &n) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
@@ -342,9 +343,37 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
             S.C = C;
             S.ct = p.ct;
             S.M = M; S.N = N; S.K = K; S.lda = lda; S.ldb = ldb; S.ldc = ldc;
+            if (o.stream_k < 0 || o.stream_k > 2) return GEMM_ERR_INVALID_VALUE;
+            const int bk = sgemm_k_step();
+            const int64_t kb = ceil_div(K, bk);
+            // Stream-K by default when it balances better than whole waves of
+            // tiles (measured from 512^3 to 8192^3, see sgemm.cu): with at
+            // most 8 waves of 128 x 128 tiles it beat the split plans by 5-29 %;
+            // the tile is the largest whose persistent CTAs still get enough
+            // K steps each (128 x 128 from 32, 128 x 64 from 8, else 64 x 64).
+            bool auto_sk = false;
+            int sk_bm = 128, sk_bn = 64;
+            if (o.stream_k == 0 && o.split_k <= 0 && o.tile_n == 0 && M > 64) {
+                const int64_t s128 = sgemm_slots(128, 128, sms, true);
+                const int64_t s64 = sgemm_slots(128, 64, sms, true);
+                if (s128 > 0 && s64 > 0) {
+                    const int64_t t128 = ceil_div(M, 128) * ceil_div(N, 128);
+                    const int64_t t64 = ceil_div(M, 128) * ceil_div(N, 64);
+                    if (t128 <= 8 * s128) {
+                        auto_sk = true;
+                        if (N > 64 && t128 * kb >= 32 * s128) {
+                            sk_bn = 128;
+                        } else if (t64 * kb < 8 * s64) {
+                            sk_bm = 64;
+                        }
+                    }
+                }
+            }
             // 128 x 64 tiles measured faster than 128 x 128 from 2048^3 to
             // 8192 x 8192 x 2048 (3 CTAs of 4 warps per SM against 2 of 8).
-            if (o.tile_n == 128) {
+            if (auto_sk) {
+                S.bm = sk_bm; S.bn = sk_bn;
+            } else if (o.tile_n == 128) {
                 S.bm = 128; S.bn = 128;
             } else if (o.tile_n == 64 || (o.tile_n == 0 && M > 64)) {
                 S.bm = 128; S.bn = 64;
@@ -354,9 +383,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
                 return GEMM_ERR_INVALID_VALUE;
             }
             if (o.split_k < 0 || o.split_k > 64) return GEMM_ERR_INVALID_VALUE;
-            const int bk = sgemm_k_step();
             const int64_t tiles = ceil_div(M, S.bm) * ceil_div(N, S.bn);
-            const int64_t kb = ceil_div(K, bk);
             const int64_t slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms));
             auto part = [&](int64_t t0, int64_t nt, int64_t splits) {
                 splits = std::max<int64_t>(1, std::min<int64_t>(splits, kb));
@@ -373,6 +400,42 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
                 }
             };
             S.nparts = 0;
+            const int64_t sk_slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms, true));
+            if (o.split_k <= 0 && (o.stream_k == 2 || auto_sk) && sk_slots > 0) {
+                // Stream-K: a persistent grid of the resident CTAs takes whole
+                // tiles while whole waves last, then shares the remaining
+                // tiles' K steps out evenly (cut tiles summed in piece order).
+                int64_t G = sk_slots;
+                int64_t dp = 0;
+                if (tiles >= G) dp = (tiles % G == 0) ? tiles : (tiles / G - 1) * G;
+                const int64_t W = (tiles - dp) * kb;
+                if (W > 0 && W < G) G = W;
+                if (W == 0) G = std::min<int64_t>(G, tiles);
+                SgemmPart& q = S.parts[S.nparts++];
+                q.tile0 = 0;
+                q.tiles = static_cast<int>(tiles);
+                q.splits = 1;
+                q.k_chunk = static_cast<int>(kb * bk);
+                q.sk_mode = 1;
+                q.dp_tiles = static_cast<int>(dp);
+                q.sk_kblocks = W;
+                q.grid = static_cast<int>(std::max<int64_t>(G, 1));
+                int max_seg = 1;
+                const int64_t sk_tiles = tiles - dp;
+                for (int64_t ts = 0; ts < sk_tiles && W > 0; ++ts) {
+                    const int64_t first = ((ts * kb + 1) * G - 1) / W;
+                    const int64_t last = (((ts + 1) * kb) * G - 1) / W;
+                    max_seg = std::max<int>(max_seg, static_cast<int>(last - first + 1));
+                }
+                q.max_seg = max_seg;
+                if (max_seg > 1) {
+                    p.ws_floats = static_cast<size_t>(sk_tiles * max_seg * S.bm * S.bn);
+                    p.n_counters = static_cast<size_t>(sk_tiles);
+                }
+                p.units = tiles;
+                *plan = p;
+                return GEMM_OK;
+            }
             if (o.split_k > 0) {
                 part(0, tiles, o.split_k);
             } else if (slots > 0 && tiles >= slots) {
@@ -589,7 +652,11 @@ void describe_kernel(const Plan& p, int dtype, char* buf, int n) {
         case Kind::Generic: snprintf(buf, n, "generic cuda-core dtype=%d tile=64x64", dtype); break;
         case Kind::Sgemm: {
             const SgemmPart& a = p.sg.parts[0];
-            if (p.sg.nparts == 1)
+            if (a.sk_mode)
+                snprintf(buf, n, "sgemm tile=%dx%dx%d stream_k tiles=%d dp_tiles=%d sk_kblocks=%lld "
+                         "max_seg=%d grid=%d", p.sg.bm, p.sg.bn, sgemm_k_step(), a.tiles, a.dp_tiles,
+                         static_cast<long long>(a.sk_kblocks), a.max_seg, a.grid);
+            else if (p.sg.nparts == 1)
                 snprintf(buf, n, "sgemm tile=%dx%dx%d tiles=%d split_k=%d units=%lld", p.sg.bm,
                          p.sg.bn, sgemm_k_step(), a.tiles, a.splits, static_cast<long long>(p.units));
             else
@@ -1006,6 +1073,15 @@ extern "C" gemm_status_t gemm_ex_noalloc(const void* A, const void* B, void* C, 
     Plan p;
     st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, *options, sms, &p);
     if (st != GEMM_OK) return st;
+    if (p.kind == Kind::Sgemm && p.sg.parts[0].sk_mode && options->stream_k == 0 &&
+        p.ws_floats * sizeof(float) > kNoallocScratchBytes - kNoallocCounterBytes) {
+        // the planner's own stream-K SGEMM needs more scratch than the array
+        // holds: plan it without stream-K (split-K waves instead)
+        gemm_options_t o2 = *options;
+        o2.stream_k = 1;
+        st = make_plan(dtype, A, B, C, M, N, K, lda, ldb, ldc, o2, sms, &p);
+        if (st != GEMM_OK) return st;
+    }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
     switch (p.kind) {
         case Kind::Nothing: return GEMM_OK;

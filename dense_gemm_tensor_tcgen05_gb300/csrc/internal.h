@@ -93,6 +93,7 @@ struct SgemmPart {
     int64_t sk_kblocks;  // stream-K: k-blocks shared out over the grid
     int max_seg;    // workspace slots per split tile per tile
     int k_chunk;    // K per slice (multiple of the kernel's K step)
+    int grid;       // stream-K: CTAs (all resident at once)
 };
 
 struct SgemmLaunch {
@@ -111,7 +112,8 @@ struct SgemmLaunch {
 };
 
 bool sgemm_tile_supported(int bm, int bn);
-cudaError_t sgemm_blocks_per_sm(int bm, int bn, int* n);
+// Resident CTAs per SM of the SGEMM kernel for a tile shape (split or stream-K form).
+cudaError_t sgemm_blocks_per_sm(int bm, int bn, bool stream_k, int* n);
 int sgemm_k_step();
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int dtype, const void* A, const void* B, void* C, int ct, int64_t M,

@@ -20,6 +20,11 @@
 // boundary tiles use guarded loads and masked stores, and only the last,
 // partial K step of any tile uses guarded loads.  Misaligned pointers or
 // leading dimensions go to the generic kernel instead.
+// Schedules: one CTA per (tile, K slice), or stream-K -- a grid of exactly
+// the CTAs that fit on the GPU at once, which first takes whole tiles while
+// whole waves of them last and then shares the remaining tiles' K steps out
+// evenly, so every SM does the same number of FMAs.  A tile cut into pieces
+// is summed by its last piece to finish, in piece order.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -28,6 +33,7 @@
 
 #include "cstore.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gb300 {
 
@@ -43,6 +49,9 @@ struct SgemmCfg {
     static constexpr int kBLoads = BK * BN / 4;    // float4 per B slice
     static constexpr int kAPer = (kALoads + kThreads - 1) / kThreads;
     static constexpr int kBPer = (kBLoads + kThreads - 1) / kThreads;
+    // resident CTAs per SM the register allocation must allow: 128 x 128 runs
+    // 2 (8 warps each), 128 x 64 runs 3 (4 warps each, <= 170 registers)
+    static constexpr int kMinBlocks = (BM * BN >= 128 * 128) ? 2 : (BM * BN >= 128 * 64) ? 3 : 1;
     static_assert(BM % 8 == 0 && BN % 8 == 0 && BK % 4 == 0, "tile shape");
     static_assert(kThreads % 32 == 0 && kThreads <= 1024, "whole warps");
     static_assert(kALoads % kThreads == 0 && kBLoads % kThreads == 0, "even load split");
@@ -64,6 +73,11 @@ struct SgArgs {
     int ct;             // C's type (cstore.cuh)
     float* ws;          // split-K partial tiles of this launch
     uint32_t* counters; // split-K arrival counter per tile, zero between launches
+    int sk_mode;        // 1: stream-K schedule (persistent grid)
+    int dp_tiles;       // stream-K: tiles done whole, tile cta, cta + grid, ...
+    int kb_total;       // stream-K: K steps (of BK) per tile
+    int64_t sk_iters;   // stream-K: K steps shared out over the grid after dp_tiles
+    int max_seg;        // stream-K: workspace slots per cut tile
 };
 
 // Load one BK slice of A (BM x BK) and B (BK x BN) starting at k0 into
@@ -264,17 +278,165 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
     }
 }
 
+// A piece of a cut tile: store this thread's partial outputs to workspace
+// slot `slot` (its 16 float4, interleaved across threads so a warp's stores
+// are contiguous) and count the arrival on the tile's counter; the piece that
+// arrives last sums the tile's `nseg` slots first_slot.. in order (fixed
+// order: the result does not depend on timing) and writes C.
+template <int BM, int BN, int BK>
+__device__ __forceinline__ void sgemm_piece(const SgArgs& a, int m0, int n0, bool edge,
+                                            float (&acc)[8][8], int64_t slot, int64_t first_slot,
+                                            int nseg, uint32_t* counter, uint32_t* s_last) {
+    using Cfg = SgemmCfg<BM, BN, BK>;
+    const int tid = threadIdx.x;
+    float4* dst = reinterpret_cast<float4*>(a.ws + slot * (BM * BN));
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        dst[q * Cfg::kThreads + tid] = make_float4(acc[q >> 1][(q & 1) * 4], acc[q >> 1][(q & 1) * 4 + 1],
+                                                   acc[q >> 1][(q & 1) * 4 + 2], acc[q >> 1][(q & 1) * 4 + 3]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(counter, 1u);
+        *s_last = (old == static_cast<uint32_t>(nseg - 1)) ? 1u : 0u;
+        if (*s_last) atomicExch(counter, 0u);   // ready for the next launch
+    }
+    __syncthreads();
+    const bool last = *s_last != 0;
+    __syncthreads();   // s_last may be reused by this CTA's next piece
+    if (!last) return;
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int s2 = 0; s2 < nseg; ++s2) {
+        const float4* src = reinterpret_cast<const float4*>(a.ws + (first_slot + s2) * (BM * BN));
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float4 v = __ldcg(src + q * Cfg::kThreads + tid);
+            acc[q >> 1][(q & 1) * 4] += v.x;
+            acc[q >> 1][(q & 1) * 4 + 1] += v.y;
+            acc[q >> 1][(q & 1) * 4 + 2] += v.z;
+            acc[q >> 1][(q & 1) * 4 + 3] += v.w;
+        }
+    }
+    if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
+    else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+}
+
+// K steps [kb0, kb1) (of BK) of tile t: the product into acc.
+template <int BM, int BN, int BK>
+__device__ __forceinline__ void sgemm_tile_range(const SgArgs& a, int t, int kb0, int kb1, float* As,
+                                                 float* Bs, float (&acc)[8][8], int& m0, int& n0,
+                                                 bool& edge) {
+    m0 = (t / a.tiles_n) * BM;
+    n0 = (t - (t / a.tiles_n) * a.tiles_n) * BN;
+    edge = !(m0 + BM <= a.M && n0 + BN <= a.N);
+    const int kbeg = kb0 * BK;
+    const int kend = min(a.K, kb1 * BK);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    if (!edge)
+        sgemm_mainloop<BM, BN, BK, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
+    else
+        sgemm_mainloop<BM, BN, BK, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
+}
+
+// The CTA covering K step x of the stream-K range (CTA c owns
+// [c*W/G, (c+1)*W/G)).
+__device__ __forceinline__ int sg_owner(int64_t x, int64_t W, int G) {
+    return static_cast<int>(((x + 1) * G - 1) / W);
+}
+
+// One stream-K segment of a CTA: K steps [kb0, kb1) of stream-K tile ts,
+// which pieces first..last (CTA indices) share.
+struct SgSeg {
+    int ts, kb0, kb1, first, last;
+};
+constexpr int kSgMaxSegs = 4;   // a CTA's share is under two tiles' K steps: at most 3 segments
+
+// Stream-K schedule: whole tiles cta, cta + G, ... below dp_tiles, then this
+// CTA's contiguous share of the remaining tiles' K steps, cut at tile edges.
+// The segments are listed in shared memory first, so that no schedule state
+// stays live in registers across the main loop.
+//
+// This form is launched with programmatic stream serialization: the grid is
+// exactly the CTAs that fit on the GPU at once, so a launch that starts while
+// the previous kernel on the stream finishes only fills the slots that kernel
+// leaves.  Listing the segments touches no global memory; every CTA waits
+// for the previous kernel (griddepcontrol.wait) before its first load.
+template <int BM, int BN, int BK>
+__device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float* Bs,
+                                               uint32_t* s_last) {
+    __shared__ SgSeg segs[kSgMaxSegs];
+    __shared__ int nsegs;
+    const int cta = blockIdx.x;
+    grid_dep_launch_dependents();
+    if (threadIdx.x == 0) {
+        const int G = gridDim.x;
+        const int64_t W = a.sk_iters, KB = a.kb_total;
+        int64_t pos = static_cast<int64_t>(cta) * W / G;
+        const int64_t end = static_cast<int64_t>(cta + 1) * W / G;
+        int n = 0;
+        while (pos < end && n < kSgMaxSegs) {
+            const int64_t ts = pos / KB;                  // tile among the stream-K tiles
+            const int64_t tile_end = (ts + 1) * KB;
+            const int64_t stop = end < tile_end ? end : tile_end;
+            SgSeg& sg = segs[n++];
+            sg.ts = static_cast<int>(ts);
+            sg.kb0 = static_cast<int>(pos - ts * KB);
+            sg.kb1 = sg.kb0 + static_cast<int>(stop - pos);
+            sg.first = sg_owner(ts * KB, W, G);
+            sg.last = sg_owner(tile_end - 1, W, G);
+            pos = stop;
+        }
+        nsegs = n;
+    }
+    grid_dep_wait();   // the previous kernel's writes (A or B may be its C) are visible
+    float acc[8][8];
+    int m0, n0;
+    bool edge;
+    for (int t = cta; t < a.dp_tiles; t += gridDim.x) {
+        sgemm_tile_range<BM, BN, BK>(a, t, 0, a.kb_total, As, Bs, acc, m0, n0, edge);
+        if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
+        else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+    }
+    __syncthreads();   // the segment list is written (the loop above may be empty)
+    for (int i = 0; i < nsegs; ++i) {
+        const SgSeg sg = segs[i];
+        sgemm_tile_range<BM, BN, BK>(a, a.dp_tiles + sg.ts, sg.kb0, sg.kb1, As, Bs, acc, m0, n0, edge);
+        const SgSeg sd = segs[i];   // re-read after the main loop instead of keeping it live
+        if (sd.first == sd.last) {
+            if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
+            else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+        } else {
+            const int64_t base = static_cast<int64_t>(sd.ts) * a.max_seg;
+            sgemm_piece<BM, BN, BK>(a, m0, n0, edge, acc, base + (cta - sd.first), base,
+                                    sd.last - sd.first + 1, a.counters + sd.ts, s_last);
+        }
+    }
+}
+
 // One CTA per (tile, K slice).  With one slice the tile goes straight to C.
 // With several, each slice stores its partial tile to the workspace and the
 // CTA that finishes last sums the partials in slice order 0..S-1 (fixed
-// order: the result does not depend on timing) and writes C.
-template <int BM, int BN, int BK>
-__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK>::kThreads, (BM * BN >= 128 * 128) ? 2 : 1)
+// order: the result does not depend on timing) and writes C.  The SK
+// instantiation runs the persistent stream-K schedule instead (a separate
+// kernel, so that its schedule costs the split kernel no registers).
+template <int BM, int BN, int BK, bool SK>
+__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK>::kThreads, SgemmCfg<BM, BN, BK>::kMinBlocks)
 sgemm_kernel(const SgArgs a) {
     using Cfg = SgemmCfg<BM, BN, BK>;
     __shared__ __align__(16) float As[2 * BK * Cfg::kAStride];
     __shared__ __align__(16) float Bs[2 * BK * BN];
     __shared__ uint32_t s_last;
+    if constexpr (SK) {
+        sgemm_stream_k<BM, BN, BK>(a, As, Bs, &s_last);
+        return;
+    }
     const int u = blockIdx.x;
     const int t = a.tile0 + u / a.splits;
     const int slice = u - (u / a.splits) * a.splits;
@@ -300,43 +462,11 @@ sgemm_kernel(const SgArgs a) {
         return;
     }
 
-    // partial tile: this thread's 16 float4, interleaved across threads so a
-    // warp's stores are contiguous
-    const int tid = threadIdx.x;
+    // partial tile of slice `slice`: slots of one tile are consecutive
     const int local_tile = u / a.splits;
-    float4* slot = reinterpret_cast<float4*>(a.ws + static_cast<int64_t>(u) * (BM * BN));
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-        slot[q * Cfg::kThreads + tid] = make_float4(acc[q >> 1][(q & 1) * 4], acc[q >> 1][(q & 1) * 4 + 1],
-                                                    acc[q >> 1][(q & 1) * 4 + 2], acc[q >> 1][(q & 1) * 4 + 3]);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t old = atomicAdd(a.counters + local_tile, 1u);
-        s_last = (old == static_cast<uint32_t>(a.splits - 1)) ? 1u : 0u;
-        if (s_last) atomicExch(a.counters + local_tile, 0u);   // ready for the next launch
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-    for (int s2 = 0; s2 < a.splits; ++s2) {
-        const float4* src = reinterpret_cast<const float4*>(
-            a.ws + (static_cast<int64_t>(local_tile) * a.splits + s2) * (BM * BN));
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const float4 v = __ldcg(src + q * Cfg::kThreads + tid);
-            acc[q >> 1][(q & 1) * 4] += v.x;
-            acc[q >> 1][(q & 1) * 4 + 1] += v.y;
-            acc[q >> 1][(q & 1) * 4 + 2] += v.z;
-            acc[q >> 1][(q & 1) * 4 + 3] += v.w;
-        }
-    }
-    if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
-    else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+    sgemm_piece<BM, BN, BK>(a, m0, n0, edge, acc, static_cast<int64_t>(u),
+                            static_cast<int64_t>(local_tile) * a.splits, a.splits,
+                            a.counters + local_tile, &s_last);
 }
 
 #ifndef GB300_SGEMM_BK
@@ -368,9 +498,31 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
         a.beta = L.beta;
         a.ws = L.ws;
         a.counters = L.counters;
-        sgemm_kernel<BM, BN, kSgemmBK>
-            <<<static_cast<unsigned>(part.tiles) * part.splits, SgemmCfg<BM, BN, kSgemmBK>::kThreads, 0,
-               stream>>>(a);
+        a.sk_mode = part.sk_mode;
+        a.dp_tiles = part.dp_tiles;
+        a.kb_total = static_cast<int>(ceil_div(L.K, kSgemmBK));
+        a.sk_iters = part.sk_kblocks;
+        a.max_seg = part.max_seg;
+        constexpr int kT = SgemmCfg<BM, BN, kSgemmBK>::kThreads;
+        if (part.sk_mode) {
+            // the persistent stream-K grid starts early beside the previous
+            // kernel (programmatic dependent launch; see sgemm_stream_k)
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(part.grid));
+            cfg.blockDim = dim3(kT);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cudaError_t e = cudaLaunchKernelEx(&cfg, sgemm_kernel<BM, BN, kSgemmBK, true>, a);
+            if (e != cudaSuccess) return e;
+        } else {
+            sgemm_kernel<BM, BN, kSgemmBK, false>
+                <<<static_cast<unsigned>(part.tiles) * part.splits, kT, 0, stream>>>(a);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -465,16 +617,17 @@ bool sgemm_tile_supported(int bm, int bn) {
     return (bm == 128 && bn == 128) || (bm == 128 && bn == 64) || (bm == 64 && bn == 64);
 }
 
-cudaError_t sgemm_blocks_per_sm(int bm, int bn, int* n) {
-    if (bm == 128 && bn == 128)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            n, sgemm_kernel<128, 128, kSgemmBK>, SgemmCfg<128, 128, kSgemmBK>::kThreads, 0);
-    if (bm == 128 && bn == 64)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            n, sgemm_kernel<128, 64, kSgemmBK>, SgemmCfg<128, 64, kSgemmBK>::kThreads, 0);
-    if (bm == 64 && bn == 64)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            n, sgemm_kernel<64, 64, kSgemmBK>, SgemmCfg<64, 64, kSgemmBK>::kThreads, 0);
+template <int BM, int BN>
+static cudaError_t blocks_per_sm(bool sk, int* n) {
+    constexpr int kT = SgemmCfg<BM, BN, kSgemmBK>::kThreads;
+    return sk ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, true>, kT, 0)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, false>, kT, 0);
+}
+
+cudaError_t sgemm_blocks_per_sm(int bm, int bn, bool stream_k, int* n) {
+    if (bm == 128 && bn == 128) return blocks_per_sm<128, 128>(stream_k, n);
+    if (bm == 128 && bn == 64) return blocks_per_sm<128, 64>(stream_k, n);
+    if (bm == 64 && bn == 64) return blocks_per_sm<64, 64>(stream_k, n);
     return cudaErrorInvalidValue;
 }
 

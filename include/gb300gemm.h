@@ -174,10 +174,14 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *   stream_k  0 = planner, 1 = off, 2 = on.  Stream-K keeps whole tiles
  *             while whole waves last and shares the remaining tiles' K range
  *             evenly over all CTAs (CTA pairs); a tile cut into pieces is
- *             summed in a fixed order.  The planner leaves it off (at the
- *             power cap, idle clusters in a partial last wave let the busy
- *             ones clock higher, which the measured shapes favour over the
- *             partial sums' traffic).  Ignored with split_k > 0.
+ *             summed in a fixed order.  For the tensor-core kernels the
+ *             planner leaves it off (at the power cap, idle clusters in a
+ *             partial last wave let the busy ones clock higher, which the
+ *             measured shapes favour over the partial sums' traffic).  For
+ *             the FP32 SGEMM it turns it on when there are at most about
+ *             eight waves of 128 x 128 tiles (M > 64), choosing the tile from
+ *             the K steps each persistent CTA gets.  Ignored with
+ *             split_k > 0.
  *   epilogue  0 = C = A x B (alpha and beta ignored); 1 = C = alpha * (A x B)
  *             + beta * C, the accumulate-onto-C form of the tensor-core
  *             operation ("04-wmma-matmul", header comment: D = A*B + C).  The

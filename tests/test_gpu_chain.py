@@ -130,3 +130,40 @@ def test_chain_write_after_read():
         assert np.array_equal(Ds[i].cpu().numpy(), want.astype(np.float32)), f"round {i}"
         Wi = oracle.encode16("f16", oracle.gemm("f16", Es[i], Ps[i]))
     assert np.array_equal(W.view(torch.int16).cpu().numpy().view(np.uint16), Wi)
+
+
+
+SG_PLANS = [{}, {"tile_n": 64, "stream_k": 2}, {"tile_n": 128, "stream_k": 2},
+            {"tile_n": 32, "stream_k": 2}, {"tile_n": 64, "split_k": 3}, {"generic": 1}]
+
+
+def test_sgemm_chain_read_after_write_and_write_after_read():
+    # FP32: X_{i+1} = X_i x P_i (read after write), with the stream-K SGEMM
+    # (programmatic dependent launch) among the plans.  A torch kernel copies
+    # each result out (read after write), and another then zeroes the input
+    # the product has just read (write after read).
+    import torch
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    M, K = 1000, 512
+    steps = 3 * len(SG_PLANS)
+    X0 = inputs.make("small_int", "f32", M, K, 31, 0)
+    Ps = []
+    for i in range(steps):
+        P = np.zeros((K, K), dtype=np.float32)
+        P[np.arange(K), np.random.default_rng(500 + i).permutation(K)] = 1.0
+        Ps.append(P)
+    Pd = [torch.from_numpy(P).cuda() for P in Ps]
+    bufs = [torch.from_numpy(X0).cuda()] + [torch.empty((M, K), device="cuda") for _ in range(steps)]
+    snaps = []
+    s = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    for i in range(steps):
+        g.gemm_ex(bufs[i].data_ptr(), Pd[i].data_ptr(), bufs[i + 1].data_ptr(), M, K, K, K, K, K,
+                  dtype=2, stream=s, **SG_PLANS[i % len(SG_PLANS)])
+        snaps.append(bufs[i + 1].clone())
+        bufs[i].zero_()
+    g.gemm_device_error(s)
+    X = X0
+    for i in range(steps):
+        X = oracle.gemm("f32", X, Ps[i]).astype(np.float32)
+        assert np.array_equal(snaps[i].cpu().numpy(), X), f"step {i}, plan {SG_PLANS[i % len(SG_PLANS)]}"

@@ -397,3 +397,23 @@ def test_plan_describe_routes():
     assert "swap=1" in plan("f16", 8, 8192, 8192)
     assert plan("f32", 4096, 4096, 4096).startswith("sgemm")
     assert plan("f16", 10, 10, 7).startswith("generic")   # lda = 7: no TMA
+
+
+@pytest.mark.parametrize("cfg", [dict(tile_n=64, stream_k=2), dict(tile_n=128, stream_k=2),
+                                 dict(tile_n=32, stream_k=2)], ids=_cfg_id)
+@pytest.mark.parametrize("shape", [(300, 520, 700), (1024, 1024, 1024), (9, 7, 3), (130, 200, 1),
+                                   (2000, 3000, 256), (64, 64, 16000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_sgemm_stream_k_exact(cfg, shape):
+    # the SGEMM's persistent stream-K grid: whole tiles, then K steps shared
+    # out evenly; cut tiles are summed by their last piece in piece order
+    M, N, K = shape
+    gu.check_full("f32", "small_int", M, N, K, exact=True, **cfg)
+    gu.check_full("f32", "uniform", M, N, K, seed=M + N + K, **cfg)
+
+
+def test_sgemm_stream_k_repeat_bit_identical():
+    A, B = gu.make_inputs("f32", "uniform", 1024, 1024, 1024, 3)
+    Cs = [gu.run_gpu("f32", A, B, 1024, 1024, 1024, tile_n=64, stream_k=2) for _ in range(3)]
+    for C in Cs[1:]:
+        assert np.array_equal(C, Cs[0])
