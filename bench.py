@@ -155,7 +155,8 @@ def load_traffic(plan: str):
 
 def kernel_name(plan: str) -> str:
     if "pair=1" in plan:
-        return "tc_gemm_pair_kernel<256, 0> (CTA pairs, 256x256 tiles, 3 stages of 2 K atoms)"
+        tail = ", the tiles after the last whole wave cut into K pieces" if "tail_split" in plan else ""
+        return f"tc_gemm_pair_kernel<256, 0> (CTA pairs, 256x256 tiles, 3 stages of 2 K atoms{tail})"
     return "tc_gemm_kernel<256, false, 0> (one CTA, 128x256 tiles)"
 
 

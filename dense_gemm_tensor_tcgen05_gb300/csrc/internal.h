@@ -32,6 +32,7 @@ struct TcLaunch {
     int sk_mode;    // 1: stream-K schedule (data-parallel tiles, then shared k-blocks)
     int dp_tiles;   // stream-K: tiles done whole
     int64_t sk_kblocks;  // stream-K: k-blocks shared out over the grid
+    int sk_ctas;    // stream-K: CTAs (clusters) sharing them, 0 = the whole grid
     int max_seg;    // workspace slots per split tile
     int group;      // raster group height in tiles along the MMA M side
     int grid;       // CTAs (persistent); <= units
@@ -55,6 +56,11 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // k-blocks on at most `sms` CTAs: fills dp_tiles, sk_kblocks, max_seg, grid
 // of L and returns the number of tiles that need workspace slots.
 int64_t tc_streamk_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sms);
+
+// Tail-split schedule: whole waves of whole tiles, then each leftover tile
+// cut into floor(sms / leftover) equal K pieces (one per CTA or cluster).
+// Fills the same fields; returns the number of cut tiles (0: plain tiles).
+int64_t tc_tailsplit_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sms);
 
 // MMA kind of an input format (0: 16-bit, 1: TF32, 2: 8-bit), its element
 // size in bytes, and the K elements one 128-byte stage row holds.

@@ -101,6 +101,7 @@ struct TcArgs {
     int32_t sk_mode;            // 1: data-parallel tiles, then stream-K over the rest
     int32_t dp_tiles;           // stream-K schedule: tiles done whole by one CTA each
     int64_t sk_kblocks;         // stream-K schedule: k-blocks shared out over the grid
+    int32_t sk_ctas;            // CTAs (pair kernel: clusters) sharing them; 0 = the whole grid
     int32_t max_seg;            // workspace slots per split tile
     int32_t group;
     int32_t ct;                 // C's type: kCF32, kCF16 or kCBF16
@@ -210,9 +211,13 @@ struct WorkIter {
     int next_u;
     int64_t pos, end;
 
+    int Gs;   // CTAs (clusters) sharing the stream-K k-blocks: 0 .. Gs-1
+
     __device__ __forceinline__ WorkIter(const TcArgs& a, int cta_, int G_) : cta(cta_), G(G_), next_u(cta_) {
-        pos = a.sk_kblocks > 0 ? static_cast<int64_t>(cta) * a.sk_kblocks / G : 0;
-        end = a.sk_kblocks > 0 ? static_cast<int64_t>(cta + 1) * a.sk_kblocks / G : 0;
+        Gs = a.sk_ctas > 0 ? a.sk_ctas : G;
+        const bool shares = a.sk_kblocks > 0 && cta < Gs;
+        pos = shares ? static_cast<int64_t>(cta) * a.sk_kblocks / Gs : 0;
+        end = shares ? static_cast<int64_t>(cta + 1) * a.sk_kblocks / Gs : 0;
     }
 
     __device__ __forceinline__ bool next(const TcArgs& a, WorkItem& it) {
@@ -246,8 +251,8 @@ struct WorkIter {
         it.tile = a.dp_tiles + static_cast<int>(ts);
         it.kb0 = static_cast<int>(pos - ts * KB);
         it.kb1 = it.kb0 + static_cast<int>(stop - pos);
-        const int first = sk_owner(ts * KB, a.sk_kblocks, G);
-        const int last = sk_owner(tile_end - 1, a.sk_kblocks, G);
+        const int first = sk_owner(ts * KB, a.sk_kblocks, Gs);
+        const int last = sk_owner(tile_end - 1, a.sk_kblocks, Gs);
         it.seg = cta - first;
         it.nseg = last - first + 1;
         it.slot = static_cast<int>(ts);
@@ -1191,6 +1196,41 @@ int64_t tc_streamk_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sm
     return max_seg > 1 ? sk_tiles : 0;
 }
 
+int64_t tc_tailsplit_schedule(TcLaunch& L, int64_t tiles, int64_t kb_total, int sms) {
+    // whole waves of whole tiles; the tiles left over (fewer than a wave) are
+    // each cut into S = floor(sms / left) equal K pieces, one per CTA, so the
+    // last wave runs S times shorter on S times as many CTAs
+    const int64_t G = sms;
+    const int64_t dp = (tiles / G) * G;
+    const int64_t left = tiles - dp;
+    const int64_t S = left > 0 ? std::min<int64_t>(G / left, kb_total) : 0;
+    L.splits = 1;
+    L.max_seg = 1;
+    L.sk_ctas = 0;
+    if (left == 0 || S < 2) {   // nothing to gain: plain whole tiles
+        L.sk_mode = 0;
+        L.dp_tiles = 0;
+        L.sk_kblocks = 0;
+        L.grid = static_cast<int>(std::min<int64_t>(tiles, G));
+        return 0;
+    }
+    const int64_t W = left * kb_total;
+    const int64_t Gs = left * S;
+    L.sk_mode = 1;
+    L.dp_tiles = static_cast<int>(dp);
+    L.sk_kblocks = W;
+    L.sk_ctas = static_cast<int>(Gs);
+    L.grid = static_cast<int>(G);
+    int max_seg = 1;
+    for (int64_t ts = 0; ts < left; ++ts) {
+        const int64_t first = ((ts * kb_total + 1) * Gs - 1) / W;
+        const int64_t last = (((ts + 1) * kb_total) * Gs - 1) / W;
+        max_seg = std::max<int>(max_seg, static_cast<int>(last - first + 1));
+    }
+    L.max_seg = max_seg;
+    return left;
+}
+
 bool tc_config_supported(int bn, int swap, int pair) {
     if (pair) return !swap && (bn == 128 || bn == 256);
     if (swap) return bn == 16 || bn == 32 || bn == 64;
@@ -1361,6 +1401,7 @@ cudaError_t tc_gemm_launch(const TcLaunch& L, EncodeTiledFn encode, cudaStream_t
     a.sk_mode = L.sk_mode;
     a.dp_tiles = L.dp_tiles;
     a.sk_kblocks = L.sk_kblocks;
+    a.sk_ctas = L.sk_ctas;
     a.max_seg = L.sk_mode ? L.max_seg : L.splits;
     a.group = L.group;
     a.ct = L.ct;

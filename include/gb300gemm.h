@@ -171,17 +171,22 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             256, no swap, no split-K).
  *   store_mode 0 = planner (tensor-core results leave through TMA stores
  *             when C's base, ldc and N allow it), 1 = plain stores.
- *   stream_k  0 = planner, 1 = off, 2 = on.  Stream-K keeps whole tiles
- *             while whole waves last and shares the remaining tiles' K range
- *             evenly over all CTAs (CTA pairs); a tile cut into pieces is
- *             summed in a fixed order.  For the tensor-core kernels the
- *             planner leaves it off (at the power cap, idle clusters in a
- *             partial last wave let the busy ones clock higher, which the
- *             measured shapes favour over the partial sums' traffic).  For
- *             the FP32 SGEMM it turns it on when there are at most about
- *             eight waves of 128 x 128 tiles (M > 64), choosing the tile from
- *             the K steps each persistent CTA gets.  Ignored with
- *             split_k > 0.
+ *   stream_k  0 = planner, 1 = off, 2 = stream-K, 3 = tail split
+ *             (tensor-core kernels only).  Stream-K keeps whole tiles while
+ *             whole waves last and shares the remaining tiles' K range
+ *             evenly over all CTAs (CTA pairs); tail split keeps whole tiles
+ *             for every whole wave and cuts each leftover tile into
+ *             floor(CTAs / leftover tiles) equal K pieces, one per CTA (CTA
+ *             pair).  A tile cut into pieces is summed in a fixed order.  For
+ *             the tensor-core kernels the planner uses tail split for the
+ *             CTA-pair kernel with at least 8 whole waves (it measured about
+ *             1 % faster at 8192^3 and slower with fewer waves) and never
+ *             stream-K (at the power cap, idle clusters in a partial last
+ *             wave let the busy ones clock higher, which the measured shapes
+ *             favour over the partial sums' traffic).  For the FP32 SGEMM it
+ *             turns stream-K on when there are at most about eight waves of
+ *             128 x 128 tiles (M > 64), choosing the tile from the K steps
+ *             each persistent CTA gets.  Ignored with split_k > 0.
  *   epilogue  0 = C = A x B (alpha and beta ignored); 1 = C = alpha * (A x B)
  *             + beta * C, the accumulate-onto-C form of the tensor-core
  *             operation ("04-wmma-matmul", header comment: D = A*B + C).  The
@@ -352,8 +357,11 @@ gemm_status_t gemm_ex_host(const void *A, const void *B, void *C,
  * Scratch: every plan that splits tiles along K keeps its partial tiles and
  * arrival counters in one static device array of GEMM_NOALLOC_SCRATCH_BYTES
  * (8 MiB: the first 64 KiB hold counters for up to 4096 tiles, the rest
- * holds partial tiles) -- the split-K and stream-K plans of the tensor-core
- * kernels (one CTA or CTA pairs) and the split-K plans of the FP32 SGEMM.
+ * holds partial tiles) -- the split-K, stream-K and tail-split plans of the
+ * tensor-core kernels (one CTA or CTA pairs) and the split-K and stream-K
+ * plans of the FP32 SGEMM.  When the planner's own choice (stream_k = 0) is
+ * a stream-K SGEMM or a tail split whose pieces do not fit, this entry point
+ * plans the product without them (split-K waves or whole tiles) instead.
  * Every GPU that loads the library holds this array until the process exits.
  * A plan whose scratch does not fit returns GEMM_ERR_INVALID_VALUE, and
  * gemm_last_cuda_error() says how much it needed.  Plans that do not split

@@ -417,3 +417,37 @@ def test_sgemm_stream_k_repeat_bit_identical():
     Cs = [gu.run_gpu("f32", A, B, 1024, 1024, 1024, tile_n=64, stream_k=2) for _ in range(3)]
     for C in Cs[1:]:
         assert np.array_equal(C, Cs[0])
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("case", [((2560, 2600, 1024), dict(cta_pair=2, stream_k=3)),
+                                  ((2560, 2048, 512), dict(cta_pair=1, tile_n=256, stream_k=3)),
+                                  ((3000, 2100, 700), dict(cta_pair=1, tile_n=128, stream_k=3)),
+                                  ((4000, 3000, 1000), dict(cta_pair=2, stream_k=3))],
+                         ids=lambda c: "x".join(map(str, c[0])) + "-" + _cfg_id(c[1]))
+def test_tail_split_exact_and_random(dt, case):
+    # whole waves of whole tiles, then the leftover tiles each cut into equal
+    # K pieces over more CTAs (or clusters), summed in piece order
+    (M, N, K), cfg = case
+    gu.check_full(dt, "small_int", M, N, K, exact=True, **cfg)
+    gu.check_full(dt, "uniform", M, N, K, seed=9, **cfg)
+
+
+def test_tail_split_plan_text():
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    args = (1 << 20, 1 << 34, 1 << 40, 2560, 2600, 1024, 1024, 2600, 2600)
+    assert "tail_split" in g.gemm_plan_describe(1, *args, cta_pair=2, stream_k=3)
+    # fewer leftover tiles than half a wave's worth is what tail split needs;
+    # a whole number of waves leaves nothing to cut
+    assert "tail_split" not in g.gemm_plan_describe(1, 1 << 20, 1 << 34, 1 << 40, 256 * 76, 256, 1024,
+                                                    1024, 256, 256, cta_pair=2, stream_k=3)
+
+
+def test_tail_split_is_the_default_from_eight_waves():
+    import dense_gemm_tensor_tcgen05_gb300 as g
+    plan = lambda n: g.gemm_plan_describe(1, 1 << 20, 1 << 34, 1 << 40, n, n, n, n, n, n)
+    assert "tail_split" in plan(8192) and "pair=1" in plan(8192)     # 13 waves + 36 tiles
+    assert "tail_split" not in plan(4096)                             # 3 waves + 28 tiles
+    assert "tail_split" not in plan(16384)                            # 53 waves + 68 tiles: S = 1
+    assert "tail_split" not in g.gemm_plan_describe(1, 1 << 20, 1 << 34, 1 << 40, 8192, 8192, 8192,
+                                                    8192, 8192, 8192, stream_k=1)

@@ -116,6 +116,24 @@ def test_noalloc_repeat_calls_allocate_nothing(L):
     assert g.gemm_alloc_count() > before
 
 
+def test_noalloc_plans_without_pieces_that_do_not_fit(L):
+    # At 8192^3 the planner's own plan cuts the 36 tiles after 13 whole waves
+    # into two K pieces each (19 MB of pieces); the scratch holds 8 MiB, so
+    # this entry point runs whole tiles instead -- the plan gemm_ex runs with
+    # stream_k = 1, bit for bit -- and the result still meets the oracle.
+    import torch
+    M = N = K = 8192
+    A, B = gu.make_inputs("bf16", "normal", M, N, K, 1238, sigma=1 / np.sqrt(K))
+    Ad, Bd = gu.to_device(A, "bf16"), gu.to_device(B, "bf16")
+    got = _call(L, "gemm_ex_noalloc", "bf16", Ad, Bd, M, N, K, dict())
+    whole = _call(L, "gemm_ex", "bf16", Ad, Bd, M, N, K, dict(stream_k=1))
+    assert np.array_equal(got, whole)
+    rows = list(range(0, 16)) + list(range(M - 16, M))
+    R = np.concatenate([oracle.gemm_rows("bf16", A, B, 0, 16), oracle.gemm_rows("bf16", A, B, M - 16, M)])
+    cmp = oracle.compare(got[rows], R, K, inputs.bits_abs_max(A, "bf16"), inputs.bits_abs_max(B, "bf16"))
+    assert cmp.ok, str(cmp)
+
+
 def test_noalloc_rejects_scratch_beyond_maximum(L):
     import torch
     M = N = K = 2048                               # 128 tiles x 8 slices x 128 KiB >> 8 MiB
