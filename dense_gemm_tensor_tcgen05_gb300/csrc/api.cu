@@ -151,18 +151,19 @@ uint64_t current_ctx_id(int dev) {
             get_id = reinterpret_cast<CtxGetIdFn>(p);
     });
     if (!get_current || !get_id) return 0;
-    CUcontext c = nullptr;
-    if (get_current(&c) != CUDA_SUCCESS) return 0;
-    if (!c) {   // cudaSetDevice initialises the primary context and makes it current
-        if (cudaSetDevice(dev) != cudaSuccess) {
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        CUcontext c = nullptr;
+        unsigned long long id = 0;
+        if (get_current(&c) == CUDA_SUCCESS && c && get_id(c, &id) == CUDA_SUCCESS)
+            return static_cast<uint64_t>(id) + 1;
+        // no context current, or one that a reset has destroyed: cudaSetDevice
+        // initialises the device's primary context and makes it current
+        if (attempt == 0 && cudaSetDevice(dev) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
-        if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
     }
-    unsigned long long id = 0;
-    if (get_id(c, &id) != CUDA_SUCCESS) return 0;
-    return static_cast<uint64_t>(id) + 1;
+    return 0;
 }
 
 // ---- split-K workspace, one per (device, stream) --------------------------------
