@@ -87,18 +87,19 @@ int pair_clusters() {
     return cache[dev];
 }
 
-// Resident SGEMM CTAs on the whole device for a tile shape and kernel form
-// (split or stream-K), cached per device.
-int sgemm_slots(int bm, int bn, int sms, bool stream_k = false) {
+// Resident SGEMM CTAs on the whole device for a tile shape, micro-tile width
+// and kernel form (split or stream-K), cached per device.
+int sgemm_slots(int bm, int bn, int sms, bool stream_k = false, int tn = 8) {
     static std::mutex mu;
-    static int cache[64][6];
+    static int cache[64][8];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const int idx = ((bm == 128 && bn == 128) ? 0 : (bm == 128 ? 1 : 2)) + (stream_k ? 3 : 0);
+    const int shape = tn == 16 ? 3 : (bm == 128 && bn == 128) ? 0 : (bm == 128 ? 1 : 2);
+    const int idx = shape + (stream_k ? 4 : 0);
     std::lock_guard<std::mutex> lk(mu);
     if (!cache[dev][idx]) {
         int n = 0;
-        if (sgemm_blocks_per_sm(bm, bn, stream_k, &n) != cudaSuccess) {
+        if (sgemm_blocks_per_sm(bm, bn, tn, stream_k, &n) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
@@ -348,11 +349,14 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
             const int bk = sgemm_k_step();
             const int64_t kb = ceil_div(K, bk);
             // Stream-K by default when it balances better than whole waves of
-            // tiles (measured from 512^3 to 8192^3, see sgemm.cu): with at
-            // most 8 waves of 128 x 128 tiles it beat the split plans by 5-29 %;
-            // the tile is the largest whose persistent CTAs still get enough
-            // K steps each (128 x 128 from 32, 128 x 64 from 8, else 64 x 64).
-            bool auto_sk = false;
+            // tiles (measured from 512^3 to 8192^3, see sgemm.cu): below 4
+            // waves of 128 x 128 tiles it beat the split plans by 5-29 %; the
+            // tile is the largest whose persistent CTAs still get enough K
+            // steps each (128 x 128 from 32, 128 x 64 from 8, else 64 x 64).
+            // From 4 waves on, whole waves of 128 x 128 tiles with 8 x 16
+            // outputs per thread (128 threads) were 0-5 % faster than both
+            // (5000^3 to 8192^3, 16384 x 4096 x 4096, 8192 x 8192 x 2048).
+            bool auto_sk = false, auto_wide = false;
             int sk_bm = 128, sk_bn = 64;
             if (o.stream_k == 0 && o.split_k <= 0 && o.tile_n == 0 && M > 64) {
                 const int64_t s128 = sgemm_slots(128, 128, sms, true);
@@ -360,20 +364,26 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
                 if (s128 > 0 && s64 > 0) {
                     const int64_t t128 = ceil_div(M, 128) * ceil_div(N, 128);
                     const int64_t t64 = ceil_div(M, 128) * ceil_div(N, 64);
-                    if (t128 <= 8 * s128) {
+                    if (t128 < 4 * s128) {
                         auto_sk = true;
                         if (N > 64 && t128 * kb >= 32 * s128) {
                             sk_bn = 128;
                         } else if (t64 * kb < 8 * s64) {
                             sk_bm = 64;
                         }
+                    } else if (N > 64) {
+                        auto_wide = true;
                     }
                 }
             }
-            // 128 x 64 tiles measured faster than 128 x 128 from 2048^3 to
-            // 8192 x 8192 x 2048 (3 CTAs of 4 warps per SM against 2 of 8).
+            // With 8 x 8 outputs per thread, 128 x 64 tiles measured faster
+            // than 128 x 128 from 2048^3 to 8192 x 8192 x 2048 (3 CTAs of 4
+            // warps per SM against 2 of 8).
+            S.tn = 8;
             if (auto_sk) {
                 S.bm = sk_bm; S.bn = sk_bn;
+            } else if (o.tile_n == 256 || auto_wide) {   // 128 x 128 tiles, 8 x 16 per thread
+                S.bm = 128; S.bn = 128; S.tn = 16;
             } else if (o.tile_n == 128) {
                 S.bm = 128; S.bn = 128;
             } else if (o.tile_n == 64 || (o.tile_n == 0 && M > 64)) {
@@ -385,7 +395,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
             }
             if (o.split_k < 0 || o.split_k > 64) return GEMM_ERR_INVALID_VALUE;
             const int64_t tiles = ceil_div(M, S.bm) * ceil_div(N, S.bn);
-            const int64_t slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms));
+            const int64_t slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms, false, S.tn));
             auto part = [&](int64_t t0, int64_t nt, int64_t splits) {
                 splits = std::max<int64_t>(1, std::min<int64_t>(splits, kb));
                 const int64_t chunk = ceil_div(ceil_div(K, splits), bk) * bk;
@@ -401,7 +411,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
                 }
             };
             S.nparts = 0;
-            const int64_t sk_slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms, true));
+            const int64_t sk_slots = static_cast<int64_t>(sgemm_slots(S.bm, S.bn, sms, true, S.tn));
             if (o.split_k <= 0 && (o.stream_k == 2 || auto_sk) && sk_slots > 0) {
                 // Stream-K: a persistent grid of the resident CTAs takes whole
                 // tiles while whole waves last, then shares the remaining
@@ -666,12 +676,14 @@ void describe_kernel(const Plan& p, int dtype, char* buf, int n) {
         case Kind::Sgemm: {
             const SgemmPart& a = p.sg.parts[0];
             if (a.sk_mode)
-                snprintf(buf, n, "sgemm tile=%dx%dx%d stream_k tiles=%d dp_tiles=%d sk_kblocks=%lld "
-                         "max_seg=%d grid=%d", p.sg.bm, p.sg.bn, sgemm_k_step(), a.tiles, a.dp_tiles,
+                snprintf(buf, n, "sgemm tile=%dx%dx%d%s stream_k tiles=%d dp_tiles=%d sk_kblocks=%lld "
+                         "max_seg=%d grid=%d", p.sg.bm, p.sg.bn, sgemm_k_step(),
+                         p.sg.tn == 16 ? " thread=8x16" : "", a.tiles, a.dp_tiles,
                          static_cast<long long>(a.sk_kblocks), a.max_seg, a.grid);
             else if (p.sg.nparts == 1)
-                snprintf(buf, n, "sgemm tile=%dx%dx%d tiles=%d split_k=%d units=%lld", p.sg.bm,
-                         p.sg.bn, sgemm_k_step(), a.tiles, a.splits, static_cast<long long>(p.units));
+                snprintf(buf, n, "sgemm tile=%dx%dx%d%s tiles=%d split_k=%d units=%lld", p.sg.bm,
+                         p.sg.bn, sgemm_k_step(), p.sg.tn == 16 ? " thread=8x16" : "", a.tiles, a.splits,
+                         static_cast<long long>(p.units));
             else
                 snprintf(buf, n, "sgemm tile=%dx%dx%d tiles=%d+%d split_k=%d+%d units=%lld",
                          p.sg.bm, p.sg.bn, sgemm_k_step(), a.tiles, p.sg.parts[1].tiles, a.splits,

@@ -109,6 +109,7 @@ struct SgemmLaunch {
     int64_t M, N, K, lda, ldb, ldc;
     int ct;             // C's type: 0 = FP32, 1 = FP16, 2 = BF16
     int bm, bn;
+    int tn;             // columns of a thread's micro-tile: 8, or 16 (128 x 128 tiles of 128 threads)
     int nparts;
     SgemmPart parts[2];
     int ab;             // 0: C = AB; 1: C = alpha AB; 2: C = alpha AB + beta C
@@ -117,9 +118,10 @@ struct SgemmLaunch {
     uint32_t* counters; // >= max over parts of tiles, zero between launches
 };
 
-bool sgemm_tile_supported(int bm, int bn);
-// Resident CTAs per SM of the SGEMM kernel for a tile shape (split or stream-K form).
-cudaError_t sgemm_blocks_per_sm(int bm, int bn, bool stream_k, int* n);
+bool sgemm_tile_supported(int bm, int bn, int tn);
+// Resident CTAs per SM of the SGEMM kernel for a tile shape and micro-tile
+// width (split or stream-K form).
+cudaError_t sgemm_blocks_per_sm(int bm, int bn, int tn, bool stream_k, int* n);
 int sgemm_k_step();
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream);
 cudaError_t generic_launch(int dtype, const void* A, const void* B, void* C, int ct, int64_t M,

@@ -6,7 +6,9 @@
 //   * a CTA computes a BM x BN tile of C; each thread owns an 8 x 8 register
 //     micro-tile split into four 4 x 4 quadrants (rows ty*4.. and BM/2+ty*4..,
 //     columns tx*4.. and BN/2+tx*4..), so every shared-memory fragment read is
-//     one float4 and a warp's reads hit distinct banks;
+//     one float4 and a warp's reads hit distinct banks.  The wide form gives
+//     each thread 8 x 16 outputs (column chunks tx*4.. + c*BN/4): 128 FMAs per
+//     6 float4 shared loads, at 128 threads per 128 x 128 tile;
 //   * per K step of BK, A (BM x BK) and B (BK x BN) slices come in with float4
 //     global loads; A is stored transposed (k-major rows of BM floats, padded
 //     by 4 so the transposing stores are conflict-free), which makes the
@@ -39,9 +41,12 @@ namespace gb300 {
 
 // ---------------------------------------------------------------- SGEMM --
 
-template <int BM, int BN, int BK>
+// TN: columns of a thread's micro-tile (8: four 4 x 4 quadrants; 16: eight
+// 4-wide column chunks), always 8 rows.
+template <int BM, int BN, int BK, int TN = 8>
 struct SgemmCfg {
-    static constexpr int kTx = BN / 8;             // threads along N
+    static constexpr int kTn = TN;
+    static constexpr int kTx = BN / TN;            // threads along N
     static constexpr int kTy = BM / 8;             // threads along M
     static constexpr int kThreads = kTx * kTy;
     static constexpr int kAStride = BM + 4;        // padded row of the transposed A slice
@@ -52,6 +57,7 @@ struct SgemmCfg {
     // resident CTAs per SM the register allocation must allow: 128 x 128 runs
     // 2 (8 warps each), 128 x 64 runs 3 (4 warps each, <= 170 registers)
     static constexpr int kMinBlocks = (BM * BN >= 128 * 128) ? 2 : (BM * BN >= 128 * 64) ? 3 : 1;
+    static_assert(TN == 8 || TN == 16, "micro-tile width");
     static_assert(BM % 8 == 0 && BN % 8 == 0 && BK % 4 == 0, "tile shape");
     static_assert(kThreads % 32 == 0 && kThreads <= 1024, "whole warps");
     static_assert(kALoads % kThreads == 0 && kBLoads % kThreads == 0, "even load split");
@@ -83,12 +89,12 @@ struct SgArgs {
 // Load one BK slice of A (BM x BK) and B (BK x BN) starting at k0 into
 // registers.  Elements at k >= kend, or outside M / N in an edge tile, read
 // as zero.
-template <int BM, int BN, int BK, bool EDGE>
+template <int BM, int BN, int BK, int TN, bool EDGE>
 __device__ __forceinline__ void sgemm_load(const SgArgs& a, int m0, int n0, int k0, int kend,
                                            bool guard_k,
-                                           float4 (&ra)[SgemmCfg<BM, BN, BK>::kAPer],
-                                           float4 (&rb)[SgemmCfg<BM, BN, BK>::kBPer]) {
-    using Cfg = SgemmCfg<BM, BN, BK>;
+                                           float4 (&ra)[SgemmCfg<BM, BN, BK, TN>::kAPer],
+                                           float4 (&rb)[SgemmCfg<BM, BN, BK, TN>::kBPer]) {
+    using Cfg = SgemmCfg<BM, BN, BK, TN>;
     const int tid = threadIdx.x;
 #pragma unroll
     for (int l = 0; l < Cfg::kAPer; ++l) {
@@ -128,11 +134,11 @@ __device__ __forceinline__ void sgemm_load(const SgArgs& a, int m0, int n0, int 
     }
 }
 
-template <int BM, int BN, int BK>
+template <int BM, int BN, int BK, int TN>
 __device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs,
-                                                 const float4 (&ra)[SgemmCfg<BM, BN, BK>::kAPer],
-                                                 const float4 (&rb)[SgemmCfg<BM, BN, BK>::kBPer]) {
-    using Cfg = SgemmCfg<BM, BN, BK>;
+                                                 const float4 (&ra)[SgemmCfg<BM, BN, BK, TN>::kAPer],
+                                                 const float4 (&rb)[SgemmCfg<BM, BN, BK, TN>::kBPer]) {
+    using Cfg = SgemmCfg<BM, BN, BK, TN>;
     const int tid = threadIdx.x;
 #pragma unroll
     for (int l = 0; l < Cfg::kAPer; ++l) {
@@ -171,25 +177,26 @@ __device__ __forceinline__ void f32x2_fma(uint64_t& acc, uint64_t a, uint64_t b)
 }
 
 // acc (this thread's 8 x 8 outputs) += A[m0.., kbeg..kend) x B[kbeg..kend, n0..)
-template <int BM, int BN, int BK, bool EDGE>
+template <int BM, int BN, int BK, int TN, bool EDGE>
 __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, int kbeg, int kend,
-                                               float* As0, float* Bs0, float (&acc)[8][8]) {
-    using Cfg = SgemmCfg<BM, BN, BK>;
+                                               float* As0, float* Bs0, float (&acc)[8][TN]) {
+    using Cfg = SgemmCfg<BM, BN, BK, TN>;
     const int tx = threadIdx.x % Cfg::kTx;
     const int ty = threadIdx.x / Cfg::kTx;
     const int k_tiles = (kend - kbeg + BK - 1) / BK;
     const int k_full = (kend - kbeg) / BK;   // slices with no K tail
 
     // accumulators as column pairs (acc[i][2p], acc[i][2p+1])
-    uint64_t acc2[8][4];
+    constexpr int kChunks = TN / 4;           // 4-wide column chunks, BN / kChunks apart
+    uint64_t acc2[8][TN / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) acc2[i][p] = f32x2_pack(acc[i][2 * p], acc[i][2 * p + 1]);
+        for (int p = 0; p < TN / 2; ++p) acc2[i][p] = f32x2_pack(acc[i][2 * p], acc[i][2 * p + 1]);
 
     float4 ra[Cfg::kAPer], rb[Cfg::kBPer];
-    sgemm_load<BM, BN, BK, EDGE>(a, m0, n0, kbeg, kend, 0 >= k_full, ra, rb);
-    sgemm_store_smem<BM, BN, BK>(As0, Bs0, ra, rb);
+    sgemm_load<BM, BN, BK, TN, EDGE>(a, m0, n0, kbeg, kend, 0 >= k_full, ra, rb);
+    sgemm_store_smem<BM, BN, BK, TN>(As0, Bs0, ra, rb);
     __syncthreads();
 
     for (int kt = 0; kt < k_tiles; ++kt) {
@@ -197,43 +204,49 @@ __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, 
         const float* Bs = Bs0 + (kt & 1) * (BK * BN);
         const bool more = kt + 1 < k_tiles;
         if (more)
-            sgemm_load<BM, BN, BK, EDGE>(a, m0, n0, kbeg + (kt + 1) * BK, kend, kt + 1 >= k_full,
+            sgemm_load<BM, BN, BK, TN, EDGE>(a, m0, n0, kbeg + (kt + 1) * BK, kend, kt + 1 >= k_full,
                                          ra, rb);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + ty * 4);
             const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + BM / 2 + ty * 4);
-            const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * BN + tx * 4);
-            const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * BN + BN / 2 + tx * 4);
+            float4 b[kChunks];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                b[c] = *reinterpret_cast<const float4*>(Bs + k * BN + c * (BN / kChunks) + tx * 4);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint64_t bp[4] = {f32x2_pack(b0.x, b0.y), f32x2_pack(b0.z, b0.w),
-                                    f32x2_pack(b1.x, b1.y), f32x2_pack(b1.z, b1.w)};
+            uint64_t bp[TN / 2];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                bp[2 * c] = f32x2_pack(b[c].x, b[c].y);
+                bp[2 * c + 1] = f32x2_pack(b[c].z, b[c].w);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint64_t ai = f32x2_pack(av[i], av[i]);
 #pragma unroll
-                for (int p = 0; p < 4; ++p) f32x2_fma(acc2[i][p], ai, bp[p]);
+                for (int p = 0; p < TN / 2; ++p) f32x2_fma(acc2[i][p], ai, bp[p]);
             }
         }
         if (more) {
             float* An = As0 + ((kt + 1) & 1) * (BK * Cfg::kAStride);
             float* Bn = Bs0 + ((kt + 1) & 1) * (BK * BN);
-            sgemm_store_smem<BM, BN, BK>(An, Bn, ra, rb);
+            sgemm_store_smem<BM, BN, BK, TN>(An, Bn, ra, rb);
         }
         __syncthreads();
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) f32x2_unpack(acc2[i][p], acc[i][2 * p], acc[i][2 * p + 1]);
+        for (int p = 0; p < TN / 2; ++p) f32x2_unpack(acc2[i][p], acc[i][2 * p], acc[i][2 * p + 1]);
 }
 
-// Quadrant (qi, qj) of the micro-tile: rows m0 + qi*BM/2 + ty*4 + i,
-// columns n0 + qj*BN/2 + tx*4 + j.
-template <int BM, int BN, int BK, bool EDGE>
+// Part (qi, qj) of the micro-tile: rows m0 + qi*BM/2 + ty*4 + i, columns
+// n0 + qj*BN/(TN/4) + tx*4 + j (TN/4 column chunks of 4).
+template <int BM, int BN, int BK, int TN, bool EDGE>
 __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
-                                              const float (&acc)[8][8]) {
-    using Cfg = SgemmCfg<BM, BN, BK>;
+                                              const float (&acc)[8][TN]) {
+    using Cfg = SgemmCfg<BM, BN, BK, TN>;
     const int tx = threadIdx.x % Cfg::kTx;
     const int ty = threadIdx.x / Cfg::kTx;
 #pragma unroll
@@ -244,8 +257,8 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
             if (EDGE && gm >= a.M) continue;
             const int64_t crow = static_cast<int64_t>(gm) * a.ldc;
 #pragma unroll
-            for (int qj = 0; qj < 2; ++qj) {
-                const int gn = n0 + qj * (BN / 2) + tx * 4;
+            for (int qj = 0; qj < TN / 4; ++qj) {
+                const int gn = n0 + qj * (BN / (TN / 4)) + tx * 4;
                 float v[4] = {acc[qi * 4 + i][qj * 4], acc[qi * 4 + i][qj * 4 + 1],
                               acc[qi * 4 + i][qj * 4 + 2], acc[qi * 4 + i][qj * 4 + 3]};
                 if (a.ab == 1) {
@@ -283,17 +296,19 @@ __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
 // are contiguous) and count the arrival on the tile's counter; the piece that
 // arrives last sums the tile's `nseg` slots first_slot.. in order (fixed
 // order: the result does not depend on timing) and writes C.
-template <int BM, int BN, int BK>
+template <int BM, int BN, int BK, int TN>
 __device__ __forceinline__ void sgemm_piece(const SgArgs& a, int m0, int n0, bool edge,
-                                            float (&acc)[8][8], int64_t slot, int64_t first_slot,
+                                            float (&acc)[8][TN], int64_t slot, int64_t first_slot,
                                             int nseg, uint32_t* counter, uint32_t* s_last) {
-    using Cfg = SgemmCfg<BM, BN, BK>;
+    using Cfg = SgemmCfg<BM, BN, BK, TN>;
     const int tid = threadIdx.x;
+    constexpr int kQ = 2 * TN;          // float4 per thread (8 rows x TN columns)
+    constexpr int kC = TN / 4;          // float4 per row
     float4* dst = reinterpret_cast<float4*>(a.ws + slot * (BM * BN));
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-        dst[q * Cfg::kThreads + tid] = make_float4(acc[q >> 1][(q & 1) * 4], acc[q >> 1][(q & 1) * 4 + 1],
-                                                   acc[q >> 1][(q & 1) * 4 + 2], acc[q >> 1][(q & 1) * 4 + 3]);
+    for (int q = 0; q < kQ; ++q)
+        dst[q * Cfg::kThreads + tid] = make_float4(acc[q / kC][(q % kC) * 4], acc[q / kC][(q % kC) * 4 + 1],
+                                                   acc[q / kC][(q % kC) * 4 + 2], acc[q / kC][(q % kC) * 4 + 3]);
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -309,26 +324,26 @@ __device__ __forceinline__ void sgemm_piece(const SgArgs& a, int m0, int n0, boo
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
     for (int s2 = 0; s2 < nseg; ++s2) {
         const float4* src = reinterpret_cast<const float4*>(a.ws + (first_slot + s2) * (BM * BN));
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < kQ; ++q) {
             const float4 v = __ldcg(src + q * Cfg::kThreads + tid);
-            acc[q >> 1][(q & 1) * 4] += v.x;
-            acc[q >> 1][(q & 1) * 4 + 1] += v.y;
-            acc[q >> 1][(q & 1) * 4 + 2] += v.z;
-            acc[q >> 1][(q & 1) * 4 + 3] += v.w;
+            acc[q / kC][(q % kC) * 4] += v.x;
+            acc[q / kC][(q % kC) * 4 + 1] += v.y;
+            acc[q / kC][(q % kC) * 4 + 2] += v.z;
+            acc[q / kC][(q % kC) * 4 + 3] += v.w;
         }
     }
-    if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
-    else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+    if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
+    else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
 }
 
 // K steps [kb0, kb1) (of BK) of tile t: the product into acc.
-template <int BM, int BN, int BK>
+template <int BM, int BN, int BK, int TN>
 __device__ __forceinline__ void sgemm_tile_range(const SgArgs& a, int t, int kb0, int kb1, float* As,
-                                                 float* Bs, float (&acc)[8][8], int& m0, int& n0,
+                                                 float* Bs, float (&acc)[8][TN], int& m0, int& n0,
                                                  bool& edge) {
     m0 = (t / a.tiles_n) * BM;
     n0 = (t - (t / a.tiles_n) * a.tiles_n) * BN;
@@ -338,11 +353,11 @@ __device__ __forceinline__ void sgemm_tile_range(const SgArgs& a, int t, int kb0
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
     if (!edge)
-        sgemm_mainloop<BM, BN, BK, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<BM, BN, BK, TN, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
     else
-        sgemm_mainloop<BM, BN, BK, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<BM, BN, BK, TN, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
 }
 
 // The CTA covering K step x of the stream-K range (CTA c owns
@@ -368,7 +383,7 @@ constexpr int kSgMaxSegs = 4;   // a CTA's share is under two tiles' K steps: at
 // the previous kernel on the stream finishes only fills the slots that kernel
 // leaves.  Listing the segments touches no global memory; every CTA waits
 // for the previous kernel (griddepcontrol.wait) before its first load.
-template <int BM, int BN, int BK>
+template <int BM, int BN, int BK, int TN>
 __device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float* Bs,
                                                uint32_t* s_last) {
     __shared__ SgSeg segs[kSgMaxSegs];
@@ -396,25 +411,25 @@ __device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float
         nsegs = n;
     }
     grid_dep_wait();   // the previous kernel's writes (A or B may be its C) are visible
-    float acc[8][8];
+    float acc[8][TN];
     int m0, n0;
     bool edge;
     for (int t = cta; t < a.dp_tiles; t += gridDim.x) {
-        sgemm_tile_range<BM, BN, BK>(a, t, 0, a.kb_total, As, Bs, acc, m0, n0, edge);
-        if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
-        else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+        sgemm_tile_range<BM, BN, BK, TN>(a, t, 0, a.kb_total, As, Bs, acc, m0, n0, edge);
+        if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
+        else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
     }
     __syncthreads();   // the segment list is written (the loop above may be empty)
     for (int i = 0; i < nsegs; ++i) {
         const SgSeg sg = segs[i];
-        sgemm_tile_range<BM, BN, BK>(a, a.dp_tiles + sg.ts, sg.kb0, sg.kb1, As, Bs, acc, m0, n0, edge);
+        sgemm_tile_range<BM, BN, BK, TN>(a, a.dp_tiles + sg.ts, sg.kb0, sg.kb1, As, Bs, acc, m0, n0, edge);
         const SgSeg sd = segs[i];   // re-read after the main loop instead of keeping it live
         if (sd.first == sd.last) {
-            if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
-            else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+            if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
+            else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
         } else {
             const int64_t base = static_cast<int64_t>(sd.ts) * a.max_seg;
-            sgemm_piece<BM, BN, BK>(a, m0, n0, edge, acc, base + (cta - sd.first), base,
+            sgemm_piece<BM, BN, BK, TN>(a, m0, n0, edge, acc, base + (cta - sd.first), base,
                                     sd.last - sd.first + 1, a.counters + sd.ts, s_last);
         }
     }
@@ -426,15 +441,15 @@ __device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float
 // order: the result does not depend on timing) and writes C.  The SK
 // instantiation runs the persistent stream-K schedule instead (a separate
 // kernel, so that its schedule costs the split kernel no registers).
-template <int BM, int BN, int BK, bool SK>
-__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK>::kThreads, SgemmCfg<BM, BN, BK>::kMinBlocks)
+template <int BM, int BN, int BK, int TN, bool SK>
+__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK, TN>::kThreads, SgemmCfg<BM, BN, BK, TN>::kMinBlocks)
 sgemm_kernel(const SgArgs a) {
-    using Cfg = SgemmCfg<BM, BN, BK>;
+    using Cfg = SgemmCfg<BM, BN, BK, TN>;
     __shared__ __align__(16) float As[2 * BK * Cfg::kAStride];
     __shared__ __align__(16) float Bs[2 * BK * BN];
     __shared__ uint32_t s_last;
     if constexpr (SK) {
-        sgemm_stream_k<BM, BN, BK>(a, As, Bs, &s_last);
+        sgemm_stream_k<BM, BN, BK, TN>(a, As, Bs, &s_last);
         return;
     }
     const int u = blockIdx.x;
@@ -446,25 +461,25 @@ sgemm_kernel(const SgArgs a) {
     const int kend = min(a.K, kbeg + a.k_chunk);
     const bool edge = !(m0 + BM <= a.M && n0 + BN <= a.N);
 
-    float acc[8][8];
+    float acc[8][TN];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
     if (!edge)
-        sgemm_mainloop<BM, BN, BK, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<BM, BN, BK, TN, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
     else
-        sgemm_mainloop<BM, BN, BK, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<BM, BN, BK, TN, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
 
     if (a.splits == 1) {
-        if (!edge) sgemm_store_c<BM, BN, BK, false>(a, m0, n0, acc);
-        else sgemm_store_c<BM, BN, BK, true>(a, m0, n0, acc);
+        if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
+        else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
         return;
     }
 
     // partial tile of slice `slice`: slots of one tile are consecutive
     const int local_tile = u / a.splits;
-    sgemm_piece<BM, BN, BK>(a, m0, n0, edge, acc, static_cast<int64_t>(u),
+    sgemm_piece<BM, BN, BK, TN>(a, m0, n0, edge, acc, static_cast<int64_t>(u),
                             static_cast<int64_t>(local_tile) * a.splits, a.splits,
                             a.counters + local_tile, &s_last);
 }
@@ -474,7 +489,7 @@ sgemm_kernel(const SgArgs a) {
 #endif
 constexpr int kSgemmBK = GB300_SGEMM_BK;
 
-template <int BM, int BN>
+template <int BM, int BN, int TN>
 static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
     for (int i = 0; i < L.nparts; ++i) {
         const SgemmPart& part = L.parts[i];
@@ -503,7 +518,7 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
         a.kb_total = static_cast<int>(ceil_div(L.K, kSgemmBK));
         a.sk_iters = part.sk_kblocks;
         a.max_seg = part.max_seg;
-        constexpr int kT = SgemmCfg<BM, BN, kSgemmBK>::kThreads;
+        constexpr int kT = SgemmCfg<BM, BN, kSgemmBK, TN>::kThreads;
         if (part.sk_mode) {
             // the persistent stream-K grid starts early beside the previous
             // kernel (programmatic dependent launch; see sgemm_stream_k)
@@ -517,10 +532,10 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            cudaError_t e = cudaLaunchKernelEx(&cfg, sgemm_kernel<BM, BN, kSgemmBK, true>, a);
+            cudaError_t e = cudaLaunchKernelEx(&cfg, sgemm_kernel<BM, BN, kSgemmBK, TN, true>, a);
             if (e != cudaSuccess) return e;
         } else {
-            sgemm_kernel<BM, BN, kSgemmBK, false>
+            sgemm_kernel<BM, BN, kSgemmBK, TN, false>
                 <<<static_cast<unsigned>(part.tiles) * part.splits, kT, 0, stream>>>(a);
         }
         cudaError_t e = cudaGetLastError();
@@ -613,30 +628,35 @@ __global__ void fill_scale_kernel(void* C, int ct, int64_t M, int64_t N, int64_t
 
 // ---------------------------------------------------------------- host --
 
-bool sgemm_tile_supported(int bm, int bn) {
-    return (bm == 128 && bn == 128) || (bm == 128 && bn == 64) || (bm == 64 && bn == 64);
+bool sgemm_tile_supported(int bm, int bn, int tn) {
+    if (tn == 16) return bm == 128 && bn == 128;
+    return tn == 8 && ((bm == 128 && bn == 128) || (bm == 128 && bn == 64) || (bm == 64 && bn == 64));
 }
 
-template <int BM, int BN>
+template <int BM, int BN, int TN>
 static cudaError_t blocks_per_sm(bool sk, int* n) {
-    constexpr int kT = SgemmCfg<BM, BN, kSgemmBK>::kThreads;
-    return sk ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, true>, kT, 0)
-              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, false>, kT, 0);
+    constexpr int kT = SgemmCfg<BM, BN, kSgemmBK, TN>::kThreads;
+    return sk ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, TN, true>, kT, 0)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, TN, false>, kT, 0);
 }
 
-cudaError_t sgemm_blocks_per_sm(int bm, int bn, bool stream_k, int* n) {
-    if (bm == 128 && bn == 128) return blocks_per_sm<128, 128>(stream_k, n);
-    if (bm == 128 && bn == 64) return blocks_per_sm<128, 64>(stream_k, n);
-    if (bm == 64 && bn == 64) return blocks_per_sm<64, 64>(stream_k, n);
+cudaError_t sgemm_blocks_per_sm(int bm, int bn, int tn, bool stream_k, int* n) {
+    if (tn == 16 && bm == 128 && bn == 128) return blocks_per_sm<128, 128, 16>(stream_k, n);
+    if (tn != 8) return cudaErrorInvalidValue;
+    if (bm == 128 && bn == 128) return blocks_per_sm<128, 128, 8>(stream_k, n);
+    if (bm == 128 && bn == 64) return blocks_per_sm<128, 64, 8>(stream_k, n);
+    if (bm == 64 && bn == 64) return blocks_per_sm<64, 64, 8>(stream_k, n);
     return cudaErrorInvalidValue;
 }
 
 int sgemm_k_step() { return kSgemmBK; }
 
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream) {
-    if (L.bm == 128 && L.bn == 128) return sgemm_go<128, 128>(L, stream);
-    if (L.bm == 128 && L.bn == 64) return sgemm_go<128, 64>(L, stream);
-    if (L.bm == 64 && L.bn == 64) return sgemm_go<64, 64>(L, stream);
+    if (L.tn == 16 && L.bm == 128 && L.bn == 128) return sgemm_go<128, 128, 16>(L, stream);
+    if (L.tn != 8) return cudaErrorInvalidValue;
+    if (L.bm == 128 && L.bn == 128) return sgemm_go<128, 128, 8>(L, stream);
+    if (L.bm == 128 && L.bn == 64) return sgemm_go<128, 64, 8>(L, stream);
+    if (L.bm == 64 && L.bn == 64) return sgemm_go<64, 64, 8>(L, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -158,8 +158,9 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             K-contiguous) and TMA-legal alignment.
  *   tile_n    dtype 0/1: tensor-core tile width along the MMA's N side: 16,
  *             32, 64, 128 or 256 (16..64 only with swap_ab = 1; 64..256
- *             without).  dtype 2: 128 -> 128x128 SGEMM tiles, 64 -> 128x64,
- *             32 -> 64x64.
+ *             without).  dtype 2: 256 -> 128x128 SGEMM tiles with 8x16
+ *             outputs per thread (128 threads), 128 -> 128x128 with 8x8
+ *             (256 threads), 64 -> 128x64, 32 -> 64x64.
  *   split_k   number of K slices, each reduced in a fixed order (1..64).
  *   swap_ab   -1 = planner, 0 = never, 1 = compute C^T = B^T A^T so that N
  *             runs along the 128-row MMA side (for small M).  The planner
@@ -184,9 +185,11 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             stream-K (at the power cap, idle clusters in a partial last
  *             wave let the busy ones clock higher, which the measured shapes
  *             favour over the partial sums' traffic).  For the FP32 SGEMM it
- *             turns stream-K on when there are at most about eight waves of
+ *             turns stream-K on when there are fewer than four waves of
  *             128 x 128 tiles (M > 64), choosing the tile from the K steps
- *             each persistent CTA gets.  Ignored with split_k > 0.
+ *             each persistent CTA gets; from four waves on it runs whole
+ *             waves of 128 x 128 tiles with 8x16 outputs per thread (N > 64).
+ *             Ignored with split_k > 0.
  *   epilogue  0 = C = A x B (alpha and beta ignored); 1 = C = alpha * (A x B)
  *             + beta * C, the accumulate-onto-C form of the tensor-core
  *             operation ("04-wmma-matmul", header comment: D = A*B + C).  The

@@ -134,7 +134,8 @@ def test_chain_write_after_read():
 
 
 SG_PLANS = [{}, {"tile_n": 64, "stream_k": 2}, {"tile_n": 128, "stream_k": 2},
-            {"tile_n": 32, "stream_k": 2}, {"tile_n": 64, "split_k": 3}, {"generic": 1}]
+            {"tile_n": 32, "stream_k": 2}, {"tile_n": 64, "split_k": 3}, {"generic": 1},
+            {"tile_n": 256}, {"tile_n": 256, "stream_k": 2}]
 
 
 def test_sgemm_chain_read_after_write_and_write_after_read():

@@ -22,6 +22,7 @@ PLANS = {
     "tc_pair_stream_k": ("f16", dict(cta_pair=2, stream_k=2)),
     "sgemm_128x64": ("f32", dict(tile_n=64)),
     "sgemm_128x128": ("f32", dict(tile_n=128)),
+    "sgemm_8x16": ("f32", dict(tile_n=256)),
     "sgemm_split": ("f32", dict(tile_n=64, split_k=3)),
     "generic_f16": ("f16", dict(generic=1)),
     "generic_f32": ("f32", dict(generic=1)),

@@ -68,7 +68,7 @@ def _draw(rng):
             o["store_mode"] = 1
     else:
         if not (o.get("trans_a") or o.get("trans_b")):
-            o["tile_n"] = int(rng.choice([0, 32, 64, 128]))
+            o["tile_n"] = int(rng.choice([0, 32, 64, 128, 256]))
             r = rng.random()
             if r < 0.3:
                 o["split_k"] = int(rng.choice([2, 3]))

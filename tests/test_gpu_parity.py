@@ -74,8 +74,8 @@ def test_tensor_core_configs_random(dt, cfg):
     gu.check_full(dt, "uniform", 333, 450, 1111, seed=5, **cfg)
 
 
-@pytest.mark.parametrize("cfg", [dict(tile_n=128), dict(tile_n=64), dict(tile_n=32)],
-                         ids=_cfg_id)
+@pytest.mark.parametrize("cfg", [dict(tile_n=256), dict(tile_n=128), dict(tile_n=64), dict(tile_n=32),
+                                 dict(tile_n=256, split_k=3)], ids=_cfg_id)
 @pytest.mark.parametrize("shape", [(300, 520, 700), (9, 7, 3), (130, 200, 1)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_sgemm_tiles_exact(cfg, shape):
@@ -400,7 +400,8 @@ def test_plan_describe_routes():
 
 
 @pytest.mark.parametrize("cfg", [dict(tile_n=64, stream_k=2), dict(tile_n=128, stream_k=2),
-                                 dict(tile_n=32, stream_k=2)], ids=_cfg_id)
+                                 dict(tile_n=32, stream_k=2), dict(tile_n=256, stream_k=2)],
+                         ids=_cfg_id)
 @pytest.mark.parametrize("shape", [(300, 520, 700), (1024, 1024, 1024), (9, 7, 3), (130, 200, 1),
                                    (2000, 3000, 256), (64, 64, 16000)],
                          ids=lambda s: "x".join(map(str, s)))
@@ -417,6 +418,19 @@ def test_sgemm_stream_k_repeat_bit_identical():
     Cs = [gu.run_gpu("f32", A, B, 1024, 1024, 1024, tile_n=64, stream_k=2) for _ in range(3)]
     for C in Cs[1:]:
         assert np.array_equal(C, Cs[0])
+
+
+@pytest.mark.parametrize("shape", [(6144, 6144, 256), (5000, 5004, 300)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_sgemm_default_wide_micro_tile_exact(shape):
+    # from four waves of 128 x 128 tiles on, the default SGEMM plan runs
+    # whole waves of tiles with 8 x 16 outputs per thread (ragged edges in
+    # the second shape)
+    M, N, K = shape
+    assert "thread=8x16" in _default_plan("f32", M, N, K), _default_plan("f32", M, N, K)
+    gu.check_full("f32", "small_int", M, N, K, exact=True)
+    gu.check_full("f32", "uniform", M, N, K, seed=M + K)
+
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
