@@ -349,13 +349,13 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
             const int bk = sgemm_k_step();
             const int64_t kb = ceil_div(K, bk);
             // Stream-K by default when it balances better than whole waves of
-            // tiles (measured from 512^3 to 8192^3, see sgemm.cu): below 4
+            // tiles (measured from 512^3 to 8192^3, see sgemm.cu): below 3
             // waves of 128 x 128 tiles it beat the split plans by 5-29 %; the
             // tile is the largest whose persistent CTAs still get enough K
             // steps each (128 x 128 from 32, 128 x 64 from 8, else 64 x 64).
-            // From 4 waves on, whole waves of 128 x 128 tiles with 8 x 16
-            // outputs per thread (128 threads) were 0-5 % faster than both
-            // (5000^3 to 8192^3, 16384 x 4096 x 4096, 8192 x 8192 x 2048).
+            // From 3 waves on, whole waves of 128 x 128 tiles with 8 x 16
+            // outputs per thread (128 threads) were 1-5 % faster than both
+            // (4096^3 to 8192^3, 16384 x 4096 x 4096, 8192 x 8192 x 2048).
             bool auto_sk = false, auto_wide = false;
             int sk_bm = 128, sk_bn = 64;
             if (o.stream_k == 0 && o.split_k <= 0 && o.tile_n == 0 && M > 64) {
@@ -364,7 +364,7 @@ gemm_status_t make_plan(int dtype, const void* A, const void* B, void* C, int64_
                 if (s128 > 0 && s64 > 0) {
                     const int64_t t128 = ceil_div(M, 128) * ceil_div(N, 128);
                     const int64_t t64 = ceil_div(M, 128) * ceil_div(N, 64);
-                    if (t128 < 4 * s128) {
+                    if (t128 < 3 * s128) {
                         auto_sk = true;
                         if (N > 64 && t128 * kb >= 32 * s128) {
                             sk_bn = 128;
@@ -685,8 +685,9 @@ void describe_kernel(const Plan& p, int dtype, char* buf, int n) {
                          p.sg.bn, sgemm_k_step(), p.sg.tn == 16 ? " thread=8x16" : "", a.tiles, a.splits,
                          static_cast<long long>(p.units));
             else
-                snprintf(buf, n, "sgemm tile=%dx%dx%d tiles=%d+%d split_k=%d+%d units=%lld",
-                         p.sg.bm, p.sg.bn, sgemm_k_step(), a.tiles, p.sg.parts[1].tiles, a.splits,
+                snprintf(buf, n, "sgemm tile=%dx%dx%d%s tiles=%d+%d split_k=%d+%d units=%lld",
+                         p.sg.bm, p.sg.bn, sgemm_k_step(), p.sg.tn == 16 ? " thread=8x16" : "", a.tiles,
+                         p.sg.parts[1].tiles, a.splits,
                          p.sg.parts[1].splits, static_cast<long long>(p.units));
             break;
         }

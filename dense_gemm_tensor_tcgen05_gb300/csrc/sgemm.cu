@@ -41,27 +41,42 @@ namespace gb300 {
 
 // ---------------------------------------------------------------- SGEMM --
 
-// TN: columns of a thread's micro-tile (8: four 4 x 4 quadrants; 16: eight
-// 4-wide column chunks), always 8 rows.
-template <int BM, int BN, int BK, int TN = 8>
+#ifndef GB300_SGEMM_BK
+#define GB300_SGEMM_BK 16
+#endif
+constexpr int kSgemmBK = GB300_SGEMM_BK;
+
+// One SGEMM configuration: a BM x BN CTA tile, K steps of BK, 8 x TN outputs
+// per thread (TN = 8 or 16).  Shared memory holds two slices (double
+// buffer); A is stored transposed, k-major rows of BM + 4 floats.  A
+// thread's rows are ty*4.. and BM/2 + ty*4.., its columns TN/4 chunks of 4:
+// c*BN/(TN/4) + tx*4.
+template <int BM_, int BN_, int BK_, int TN_>
 struct SgemmCfg {
-    static constexpr int kTn = TN;
+    static constexpr int BM = BM_, BN = BN_, BK = BK_, TN = TN_;
     static constexpr int kTx = BN / TN;            // threads along N
     static constexpr int kTy = BM / 8;             // threads along M
     static constexpr int kThreads = kTx * kTy;
+    static constexpr int kChunks = TN / 4;         // 4-wide column chunks per thread
     static constexpr int kAStride = BM + 4;        // padded row of the transposed A slice
+    static constexpr int kAFloats = BK * kAStride; // one A slice
+    static constexpr int kBFloats = BK * BN;       // one B slice
+    static constexpr int kSmemBytes = 2 * (kAFloats + kBFloats) * 4;
     static constexpr int kALoads = BM * BK / 4;    // float4 per A slice
     static constexpr int kBLoads = BK * BN / 4;    // float4 per B slice
-    static constexpr int kAPer = (kALoads + kThreads - 1) / kThreads;
-    static constexpr int kBPer = (kBLoads + kThreads - 1) / kThreads;
+    static constexpr int kAPer = kALoads / kThreads;
+    static constexpr int kBPer = kBLoads / kThreads;
     // resident CTAs per SM the register allocation must allow: 128 x 128 runs
-    // 2 (8 warps each), 128 x 64 runs 3 (4 warps each, <= 170 registers)
+    // 2, 128 x 64 runs 3 (4 warps each, <= 170 registers)
     static constexpr int kMinBlocks = (BM * BN >= 128 * 128) ? 2 : (BM * BN >= 128 * 64) ? 3 : 1;
     static_assert(TN == 8 || TN == 16, "micro-tile width");
-    static_assert(BM % 8 == 0 && BN % 8 == 0 && BK % 4 == 0, "tile shape");
+    static_assert(BM % 8 == 0 && BN % TN == 0 && BK % 4 == 0, "tile shape");
     static_assert(kThreads % 32 == 0 && kThreads <= 1024, "whole warps");
     static_assert(kALoads % kThreads == 0 && kBLoads % kThreads == 0, "even load split");
-    static_assert(2 * (BK * kAStride + BK * BN) * 4 <= 48 * 1024, "static shared memory");
+    static_assert(kAFloats % 4 == 0, "16-byte aligned buffers");
+
+    __device__ static __forceinline__ int row(int ty, int i) { return (i >> 2) * (BM / 2) + ty * 4 + (i & 3); }
+    __device__ static __forceinline__ int col(int tx, int c) { return c * (BN / kChunks) + tx * 4; }
 };
 
 struct SgArgs {
@@ -86,15 +101,31 @@ struct SgArgs {
     int max_seg;        // stream-K: workspace slots per cut tile
 };
 
+// Packed FP32 pairs: fma.rn.f32x2 performs two independent single-rounding
+// FMAs, the same arithmetic as two fmaf, in one instruction -- half the
+// issue slots of the inner loop, which is what bounds this kernel.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ void f32x2_fma(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
 // Load one BK slice of A (BM x BK) and B (BK x BN) starting at k0 into
 // registers.  Elements at k >= kend, or outside M / N in an edge tile, read
 // as zero.
-template <int BM, int BN, int BK, int TN, bool EDGE>
+template <class Cfg, bool EDGE>
 __device__ __forceinline__ void sgemm_load(const SgArgs& a, int m0, int n0, int k0, int kend,
-                                           bool guard_k,
-                                           float4 (&ra)[SgemmCfg<BM, BN, BK, TN>::kAPer],
-                                           float4 (&rb)[SgemmCfg<BM, BN, BK, TN>::kBPer]) {
-    using Cfg = SgemmCfg<BM, BN, BK, TN>;
+                                           bool guard_k, float4 (&ra)[Cfg::kAPer],
+                                           float4 (&rb)[Cfg::kBPer]) {
+    constexpr int BK = Cfg::BK, BN = Cfg::BN;
     const int tid = threadIdx.x;
 #pragma unroll
     for (int l = 0; l < Cfg::kAPer; ++l) {
@@ -134,11 +165,10 @@ __device__ __forceinline__ void sgemm_load(const SgArgs& a, int m0, int n0, int 
     }
 }
 
-template <int BM, int BN, int BK, int TN>
-__device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs,
-                                                 const float4 (&ra)[SgemmCfg<BM, BN, BK, TN>::kAPer],
-                                                 const float4 (&rb)[SgemmCfg<BM, BN, BK, TN>::kBPer]) {
-    using Cfg = SgemmCfg<BM, BN, BK, TN>;
+template <class Cfg>
+__device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs, const float4 (&ra)[Cfg::kAPer],
+                                                 const float4 (&rb)[Cfg::kBPer]) {
+    constexpr int BK = Cfg::BK, BN = Cfg::BN;
     const int tid = threadIdx.x;
 #pragma unroll
     for (int l = 0; l < Cfg::kAPer; ++l) {
@@ -159,80 +189,86 @@ __device__ __forceinline__ void sgemm_store_smem(float* As, float* Bs,
     }
 }
 
-// Packed FP32 pairs: fma.rn.f32x2 performs two independent single-rounding
-// FMAs, the same arithmetic as two fmaf, in one instruction -- half the
-// issue slots of the inner loop, which is what bounds this kernel.
-__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
+// acc2 (this thread's outputs as column pairs) += one BK slice from shared
+// memory.  With PF the fragments of step k + 1 are read before the FMAs of
+// step k (two register sets); without it each step reads its own.  PF
+// measured 1-7 % faster for the split kernel's whole tiles and 2-4 % slower
+// for the stream-K form, which uses it off.
+template <class Cfg, bool PF>
+__device__ __forceinline__ void sgemm_slice(const float* As, const float* Bs, int tx, int ty,
+                                            uint64_t (&acc2)[8][Cfg::TN / 2]) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, TN = Cfg::TN;
+    float4 fa[2][2], fb[2][Cfg::kChunks];
+    auto load = [&](int k, int s) {
+        fa[s][0] = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + ty * 4);
+        fa[s][1] = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + BM / 2 + ty * 4);
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c)
+            fb[s][c] = *reinterpret_cast<const float4*>(Bs + k * BN + Cfg::col(tx, c));
+    };
+    if constexpr (PF) load(0, 0);
+#pragma unroll
+    for (int k = 0; k < Cfg::BK; ++k) {
+        const int s = PF ? (k & 1) : 0;
+        if constexpr (PF) {
+            if (k + 1 < Cfg::BK) load(k + 1, s ^ 1);
+        } else {
+            load(k, 0);
+        }
+        const float av[8] = {fa[s][0].x, fa[s][0].y, fa[s][0].z, fa[s][0].w,
+                             fa[s][1].x, fa[s][1].y, fa[s][1].z, fa[s][1].w};
+        uint64_t bp[TN / 2];
+#pragma unroll
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+            bp[2 * c] = f32x2_pack(fb[s][c].x, fb[s][c].y);
+            bp[2 * c + 1] = f32x2_pack(fb[s][c].z, fb[s][c].w);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint64_t ai = f32x2_pack(av[i], av[i]);
+#pragma unroll
+            for (int p = 0; p < TN / 2; ++p) f32x2_fma(acc2[i][p], ai, bp[p]);
+        }
+    }
 }
 
-__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ void f32x2_fma(uint64_t& acc, uint64_t a, uint64_t b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-
-// acc (this thread's 8 x 8 outputs) += A[m0.., kbeg..kend) x B[kbeg..kend, n0..)
-template <int BM, int BN, int BK, int TN, bool EDGE>
+// acc (this thread's 8 x TN outputs) += A[m0.., kbeg..kend) x B[kbeg..kend, n0..).
+// Two shared-memory buffers: the next slice is loaded into registers while
+// the current one is multiplied, then stored to the other buffer, with one
+// barrier per slice.  Ends with a barrier, so the caller may reuse shared
+// memory.
+template <class Cfg, bool EDGE, bool PF>
 __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, int kbeg, int kend,
-                                               float* As0, float* Bs0, float (&acc)[8][TN]) {
-    using Cfg = SgemmCfg<BM, BN, BK, TN>;
+                                               float* smem, float (&acc)[8][Cfg::TN]) {
+    constexpr int BK = Cfg::BK, TN = Cfg::TN;
     const int tx = threadIdx.x % Cfg::kTx;
     const int ty = threadIdx.x / Cfg::kTx;
     const int k_tiles = (kend - kbeg + BK - 1) / BK;
     const int k_full = (kend - kbeg) / BK;   // slices with no K tail
 
     // accumulators as column pairs (acc[i][2p], acc[i][2p+1])
-    constexpr int kChunks = TN / 4;           // 4-wide column chunks, BN / kChunks apart
     uint64_t acc2[8][TN / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int p = 0; p < TN / 2; ++p) acc2[i][p] = f32x2_pack(acc[i][2 * p], acc[i][2 * p + 1]);
 
+    float* As0 = smem;
+    float* Bs0 = smem + 2 * Cfg::kAFloats;
     float4 ra[Cfg::kAPer], rb[Cfg::kBPer];
-    sgemm_load<BM, BN, BK, TN, EDGE>(a, m0, n0, kbeg, kend, 0 >= k_full, ra, rb);
-    sgemm_store_smem<BM, BN, BK, TN>(As0, Bs0, ra, rb);
+    sgemm_load<Cfg, EDGE>(a, m0, n0, kbeg, kend, 0 >= k_full, ra, rb);
+    sgemm_store_smem<Cfg>(As0, Bs0, ra, rb);
     __syncthreads();
-
     for (int kt = 0; kt < k_tiles; ++kt) {
-        const float* As = As0 + (kt & 1) * (BK * Cfg::kAStride);
-        const float* Bs = Bs0 + (kt & 1) * (BK * BN);
+        const float* As = As0 + (kt & 1) * Cfg::kAFloats;
+        const float* Bs = Bs0 + (kt & 1) * Cfg::kBFloats;
         const bool more = kt + 1 < k_tiles;
         if (more)
-            sgemm_load<BM, BN, BK, TN, EDGE>(a, m0, n0, kbeg + (kt + 1) * BK, kend, kt + 1 >= k_full,
-                                         ra, rb);
-#pragma unroll
-        for (int k = 0; k < BK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + ty * 4);
-            const float4 a1 = *reinterpret_cast<const float4*>(As + k * Cfg::kAStride + BM / 2 + ty * 4);
-            float4 b[kChunks];
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                b[c] = *reinterpret_cast<const float4*>(Bs + k * BN + c * (BN / kChunks) + tx * 4);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            uint64_t bp[TN / 2];
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                bp[2 * c] = f32x2_pack(b[c].x, b[c].y);
-                bp[2 * c + 1] = f32x2_pack(b[c].z, b[c].w);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint64_t ai = f32x2_pack(av[i], av[i]);
-#pragma unroll
-                for (int p = 0; p < TN / 2; ++p) f32x2_fma(acc2[i][p], ai, bp[p]);
-            }
-        }
-        if (more) {
-            float* An = As0 + ((kt + 1) & 1) * (BK * Cfg::kAStride);
-            float* Bn = Bs0 + ((kt + 1) & 1) * (BK * BN);
-            sgemm_store_smem<BM, BN, BK, TN>(An, Bn, ra, rb);
-        }
+            sgemm_load<Cfg, EDGE>(a, m0, n0, kbeg + (kt + 1) * BK, kend, kt + 1 >= k_full, ra, rb);
+        sgemm_slice<Cfg, PF>(As, Bs, tx, ty, acc2);
+        if (more)
+            sgemm_store_smem<Cfg>(As0 + ((kt + 1) & 1) * Cfg::kAFloats, Bs0 + ((kt + 1) & 1) * Cfg::kBFloats,
+                                  ra, rb);
         __syncthreads();
     }
 #pragma unroll
@@ -241,70 +277,66 @@ __device__ __forceinline__ void sgemm_mainloop(const SgArgs& a, int m0, int n0, 
         for (int p = 0; p < TN / 2; ++p) f32x2_unpack(acc2[i][p], acc[i][2 * p], acc[i][2 * p + 1]);
 }
 
-// Part (qi, qj) of the micro-tile: rows m0 + qi*BM/2 + ty*4 + i, columns
-// n0 + qj*BN/(TN/4) + tx*4 + j (TN/4 column chunks of 4).
-template <int BM, int BN, int BK, int TN, bool EDGE>
+// This thread's outputs to C: row m0 + Cfg::row(ty, i), columns
+// n0 + Cfg::col(tx, c) + 0..3, through the epilogue (alpha, beta, C type).
+template <class Cfg, bool EDGE>
 __device__ __forceinline__ void sgemm_store_c(const SgArgs& a, int m0, int n0,
-                                              const float (&acc)[8][TN]) {
-    using Cfg = SgemmCfg<BM, BN, BK, TN>;
+                                              const float (&acc)[8][Cfg::TN]) {
     const int tx = threadIdx.x % Cfg::kTx;
     const int ty = threadIdx.x / Cfg::kTx;
 #pragma unroll
-    for (int qi = 0; qi < 2; ++qi) {
+    for (int i = 0; i < 8; ++i) {
+        const int gm = m0 + Cfg::row(ty, i);
+        if (EDGE && gm >= a.M) continue;
+        const int64_t crow = static_cast<int64_t>(gm) * a.ldc;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int gm = m0 + qi * (BM / 2) + ty * 4 + i;
-            if (EDGE && gm >= a.M) continue;
-            const int64_t crow = static_cast<int64_t>(gm) * a.ldc;
+        for (int c = 0; c < Cfg::kChunks; ++c) {
+            const int gn = n0 + Cfg::col(tx, c);
+            float v[4] = {acc[i][c * 4], acc[i][c * 4 + 1], acc[i][c * 4 + 2], acc[i][c * 4 + 3]};
+            if (a.ab == 1) {
 #pragma unroll
-            for (int qj = 0; qj < TN / 4; ++qj) {
-                const int gn = n0 + qj * (BN / (TN / 4)) + tx * 4;
-                float v[4] = {acc[qi * 4 + i][qj * 4], acc[qi * 4 + i][qj * 4 + 1],
-                              acc[qi * 4 + i][qj * 4 + 2], acc[qi * 4 + i][qj * 4 + 3]};
-                if (a.ab == 1) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] *= a.alpha;
-                } else if (a.ab == 2) {
-                    // alpha * AB + beta * C, reading C only inside it
-                    if (!EDGE) {
-                        const float4 c = c_load4(a.C, crow + gn, a.ct);
-                        v[0] = fmaf(a.alpha, v[0], a.beta * c.x);
-                        v[1] = fmaf(a.alpha, v[1], a.beta * c.y);
-                        v[2] = fmaf(a.alpha, v[2], a.beta * c.z);
-                        v[3] = fmaf(a.alpha, v[3], a.beta * c.w);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            v[j] = fmaf(a.alpha, v[j],
-                                        (gn + j < a.N) ? a.beta * c_load(a.C, crow + gn + j, a.ct) : 0.0f);
-                    }
-                }
+                for (int j = 0; j < 4; ++j) v[j] *= a.alpha;
+            } else if (a.ab == 2) {
+                // alpha * AB + beta * C, reading C only inside it
                 if (!EDGE) {
-                    c_store4(a.C, crow + gn, v[0], v[1], v[2], v[3], a.ct);
+                    const float4 cv = c_load4(a.C, crow + gn, a.ct);
+                    v[0] = fmaf(a.alpha, v[0], a.beta * cv.x);
+                    v[1] = fmaf(a.alpha, v[1], a.beta * cv.y);
+                    v[2] = fmaf(a.alpha, v[2], a.beta * cv.z);
+                    v[3] = fmaf(a.alpha, v[3], a.beta * cv.w);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (gn + j < a.N) c_store(a.C, crow + gn + j, v[j], a.ct);
+                        v[j] = fmaf(a.alpha, v[j],
+                                    (gn + j < a.N) ? a.beta * c_load(a.C, crow + gn + j, a.ct) : 0.0f);
                 }
+            }
+            if (!EDGE) {
+                c_store4(a.C, crow + gn, v[0], v[1], v[2], v[3], a.ct);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gn + j < a.N) c_store(a.C, crow + gn + j, v[j], a.ct);
             }
         }
     }
 }
 
 // A piece of a cut tile: store this thread's partial outputs to workspace
-// slot `slot` (its 16 float4, interleaved across threads so a warp's stores
-// are contiguous) and count the arrival on the tile's counter; the piece that
-// arrives last sums the tile's `nseg` slots first_slot.. in order (fixed
-// order: the result does not depend on timing) and writes C.
-template <int BM, int BN, int BK, int TN>
+// slot `slot` (its 2*TN float4, interleaved across threads so a warp's
+// stores are contiguous) and count the arrival on the tile's counter; the
+// piece that arrives last sums the tile's `nseg` slots first_slot.. in order
+// (fixed order: the result does not depend on timing) and writes C.
+template <class Cfg>
 __device__ __forceinline__ void sgemm_piece(const SgArgs& a, int m0, int n0, bool edge,
-                                            float (&acc)[8][TN], int64_t slot, int64_t first_slot,
+                                            float (&acc)[8][Cfg::TN], int64_t slot, int64_t first_slot,
                                             int nseg, uint32_t* counter, uint32_t* s_last) {
-    using Cfg = SgemmCfg<BM, BN, BK, TN>;
+    constexpr int TN = Cfg::TN;
     const int tid = threadIdx.x;
     constexpr int kQ = 2 * TN;          // float4 per thread (8 rows x TN columns)
     constexpr int kC = TN / 4;          // float4 per row
-    float4* dst = reinterpret_cast<float4*>(a.ws + slot * (BM * BN));
+    constexpr int64_t kTile = Cfg::BM * Cfg::BN;
+    float4* dst = reinterpret_cast<float4*>(a.ws + slot * kTile);
 #pragma unroll
     for (int q = 0; q < kQ; ++q)
         dst[q * Cfg::kThreads + tid] = make_float4(acc[q / kC][(q % kC) * 4], acc[q / kC][(q % kC) * 4 + 1],
@@ -326,7 +358,7 @@ __device__ __forceinline__ void sgemm_piece(const SgArgs& a, int m0, int n0, boo
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
     for (int s2 = 0; s2 < nseg; ++s2) {
-        const float4* src = reinterpret_cast<const float4*>(a.ws + (first_slot + s2) * (BM * BN));
+        const float4* src = reinterpret_cast<const float4*>(a.ws + (first_slot + s2) * kTile);
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
             const float4 v = __ldcg(src + q * Cfg::kThreads + tid);
@@ -336,28 +368,28 @@ __device__ __forceinline__ void sgemm_piece(const SgArgs& a, int m0, int n0, boo
             acc[q / kC][(q % kC) * 4 + 3] += v.w;
         }
     }
-    if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
-    else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
+    if (!edge) sgemm_store_c<Cfg, false>(a, m0, n0, acc);
+    else sgemm_store_c<Cfg, true>(a, m0, n0, acc);
 }
 
-// K steps [kb0, kb1) (of BK) of tile t: the product into acc.
-template <int BM, int BN, int BK, int TN>
-__device__ __forceinline__ void sgemm_tile_range(const SgArgs& a, int t, int kb0, int kb1, float* As,
-                                                 float* Bs, float (&acc)[8][TN], int& m0, int& n0,
+// K steps [kb0, kb1) (of BK) of tile t: the product into acc (stream-K form).
+template <class Cfg>
+__device__ __forceinline__ void sgemm_tile_range(const SgArgs& a, int t, int kb0, int kb1, float* smem,
+                                                 float (&acc)[8][Cfg::TN], int& m0, int& n0,
                                                  bool& edge) {
-    m0 = (t / a.tiles_n) * BM;
-    n0 = (t - (t / a.tiles_n) * a.tiles_n) * BN;
-    edge = !(m0 + BM <= a.M && n0 + BN <= a.N);
-    const int kbeg = kb0 * BK;
-    const int kend = min(a.K, kb1 * BK);
+    m0 = (t / a.tiles_n) * Cfg::BM;
+    n0 = (t - (t / a.tiles_n) * a.tiles_n) * Cfg::BN;
+    const int kbeg = kb0 * Cfg::BK;
+    const int kend = min(a.K, kb1 * Cfg::BK);
+    edge = !(m0 + Cfg::BM <= a.M && n0 + Cfg::BN <= a.N);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = 0.0f;
     if (!edge)
-        sgemm_mainloop<BM, BN, BK, TN, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<Cfg, false, false>(a, m0, n0, kbeg, kend, smem, acc);
     else
-        sgemm_mainloop<BM, BN, BK, TN, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<Cfg, true, false>(a, m0, n0, kbeg, kend, smem, acc);
 }
 
 // The CTA covering K step x of the stream-K range (CTA c owns
@@ -383,9 +415,8 @@ constexpr int kSgMaxSegs = 4;   // a CTA's share is under two tiles' K steps: at
 // the previous kernel on the stream finishes only fills the slots that kernel
 // leaves.  Listing the segments touches no global memory; every CTA waits
 // for the previous kernel (griddepcontrol.wait) before its first load.
-template <int BM, int BN, int BK, int TN>
-__device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float* Bs,
-                                               uint32_t* s_last) {
+template <class Cfg>
+__device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* smem, uint32_t* s_last) {
     __shared__ SgSeg segs[kSgMaxSegs];
     __shared__ int nsegs;
     const int cta = blockIdx.x;
@@ -411,26 +442,26 @@ __device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float
         nsegs = n;
     }
     grid_dep_wait();   // the previous kernel's writes (A or B may be its C) are visible
-    float acc[8][TN];
+    float acc[8][Cfg::TN];
     int m0, n0;
     bool edge;
     for (int t = cta; t < a.dp_tiles; t += gridDim.x) {
-        sgemm_tile_range<BM, BN, BK, TN>(a, t, 0, a.kb_total, As, Bs, acc, m0, n0, edge);
-        if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
-        else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
+        sgemm_tile_range<Cfg>(a, t, 0, a.kb_total, smem, acc, m0, n0, edge);
+        if (!edge) sgemm_store_c<Cfg, false>(a, m0, n0, acc);
+        else sgemm_store_c<Cfg, true>(a, m0, n0, acc);
     }
     __syncthreads();   // the segment list is written (the loop above may be empty)
     for (int i = 0; i < nsegs; ++i) {
         const SgSeg sg = segs[i];
-        sgemm_tile_range<BM, BN, BK, TN>(a, a.dp_tiles + sg.ts, sg.kb0, sg.kb1, As, Bs, acc, m0, n0, edge);
+        sgemm_tile_range<Cfg>(a, a.dp_tiles + sg.ts, sg.kb0, sg.kb1, smem, acc, m0, n0, edge);
         const SgSeg sd = segs[i];   // re-read after the main loop instead of keeping it live
         if (sd.first == sd.last) {
-            if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
-            else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
+            if (!edge) sgemm_store_c<Cfg, false>(a, m0, n0, acc);
+            else sgemm_store_c<Cfg, true>(a, m0, n0, acc);
         } else {
             const int64_t base = static_cast<int64_t>(sd.ts) * a.max_seg;
-            sgemm_piece<BM, BN, BK, TN>(a, m0, n0, edge, acc, base + (cta - sd.first), base,
-                                    sd.last - sd.first + 1, a.counters + sd.ts, s_last);
+            sgemm_piece<Cfg>(a, m0, n0, edge, acc, base + (cta - sd.first), base, sd.last - sd.first + 1,
+                             a.counters + sd.ts, s_last);
         }
     }
 }
@@ -441,55 +472,57 @@ __device__ __forceinline__ void sgemm_stream_k(const SgArgs& a, float* As, float
 // order: the result does not depend on timing) and writes C.  The SK
 // instantiation runs the persistent stream-K schedule instead (a separate
 // kernel, so that its schedule costs the split kernel no registers).
-template <int BM, int BN, int BK, int TN, bool SK>
-__global__ void __launch_bounds__(SgemmCfg<BM, BN, BK, TN>::kThreads, SgemmCfg<BM, BN, BK, TN>::kMinBlocks)
-sgemm_kernel(const SgArgs a) {
-    using Cfg = SgemmCfg<BM, BN, BK, TN>;
-    __shared__ __align__(16) float As[2 * BK * Cfg::kAStride];
-    __shared__ __align__(16) float Bs[2 * BK * BN];
+// Shared memory (the operand buffers) is dynamic: Cfg::kSmemBytes.
+template <class Cfg, bool SK>
+__global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks) sgemm_kernel(const SgArgs a) {
+    extern __shared__ __align__(16) float sg_smem[];
     __shared__ uint32_t s_last;
     if constexpr (SK) {
-        sgemm_stream_k<BM, BN, BK, TN>(a, As, Bs, &s_last);
+        sgemm_stream_k<Cfg>(a, sg_smem, &s_last);
         return;
     }
     const int u = blockIdx.x;
-    const int t = a.tile0 + u / a.splits;
-    const int slice = u - (u / a.splits) * a.splits;
-    const int m0 = (t / a.tiles_n) * BM;
-    const int n0 = (t - (t / a.tiles_n) * a.tiles_n) * BN;
+    const int tile = a.tile0 + u / a.splits;
+    const int slice = u % a.splits;
+    const int m0 = (tile / a.tiles_n) * Cfg::BM;
+    const int n0 = (tile % a.tiles_n) * Cfg::BN;
     const int kbeg = slice * a.k_chunk;
     const int kend = min(a.K, kbeg + a.k_chunk);
-    const bool edge = !(m0 + BM <= a.M && n0 + BN <= a.N);
+    const bool edge = !(m0 + Cfg::BM <= a.M && n0 + Cfg::BN <= a.N);
 
-    float acc[8][TN];
+    float acc[8][Cfg::TN];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = 0.0f;
     if (!edge)
-        sgemm_mainloop<BM, BN, BK, TN, false>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<Cfg, false, true>(a, m0, n0, kbeg, kend, sg_smem, acc);
     else
-        sgemm_mainloop<BM, BN, BK, TN, true>(a, m0, n0, kbeg, kend, As, Bs, acc);
+        sgemm_mainloop<Cfg, true, true>(a, m0, n0, kbeg, kend, sg_smem, acc);
 
     if (a.splits == 1) {
-        if (!edge) sgemm_store_c<BM, BN, BK, TN, false>(a, m0, n0, acc);
-        else sgemm_store_c<BM, BN, BK, TN, true>(a, m0, n0, acc);
+        if (!edge) sgemm_store_c<Cfg, false>(a, m0, n0, acc);
+        else sgemm_store_c<Cfg, true>(a, m0, n0, acc);
         return;
     }
 
     // partial tile of slice `slice`: slots of one tile are consecutive
     const int local_tile = u / a.splits;
-    sgemm_piece<BM, BN, BK, TN>(a, m0, n0, edge, acc, static_cast<int64_t>(u),
-                            static_cast<int64_t>(local_tile) * a.splits, a.splits,
-                            a.counters + local_tile, &s_last);
+    sgemm_piece<Cfg>(a, m0, n0, edge, acc, static_cast<int64_t>(u),
+                     static_cast<int64_t>(local_tile) * a.splits, a.splits, a.counters + local_tile,
+                     &s_last);
 }
 
-#ifndef GB300_SGEMM_BK
-#define GB300_SGEMM_BK 16
-#endif
-constexpr int kSgemmBK = GB300_SGEMM_BK;
+// Dynamic shared memory above 48 KB must be requested for the kernel (on
+// the current device, before each launch: the setting belongs to a context).
+template <class Cfg, bool SK>
+static cudaError_t sgemm_prepare() {
+    if (Cfg::kSmemBytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(sgemm_kernel<Cfg, SK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::kSmemBytes);
+}
 
-template <int BM, int BN, int TN>
+template <class Cfg>
 static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
     for (int i = 0; i < L.nparts; ++i) {
         const SgemmPart& part = L.parts[i];
@@ -504,7 +537,7 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
         a.ldb = L.ldb;
         a.ldc = L.ldc;
         a.ct = L.ct;
-        a.tiles_n = static_cast<int>(ceil_div(L.N, BN));
+        a.tiles_n = static_cast<int>(ceil_div(L.N, Cfg::BN));
         a.tile0 = part.tile0;
         a.splits = part.splits;
         a.k_chunk = part.k_chunk;
@@ -518,25 +551,28 @@ static cudaError_t sgemm_go(const SgemmLaunch& L, cudaStream_t stream) {
         a.kb_total = static_cast<int>(ceil_div(L.K, kSgemmBK));
         a.sk_iters = part.sk_kblocks;
         a.max_seg = part.max_seg;
-        constexpr int kT = SgemmCfg<BM, BN, kSgemmBK, TN>::kThreads;
         if (part.sk_mode) {
+            cudaError_t e = sgemm_prepare<Cfg, true>();
+            if (e != cudaSuccess) return e;
             // the persistent stream-K grid starts early beside the previous
             // kernel (programmatic dependent launch; see sgemm_stream_k)
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(static_cast<unsigned>(part.grid));
-            cfg.blockDim = dim3(kT);
-            cfg.dynamicSmemBytes = 0;
+            cfg.blockDim = dim3(Cfg::kThreads);
+            cfg.dynamicSmemBytes = Cfg::kSmemBytes;
             cfg.stream = stream;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            cudaError_t e = cudaLaunchKernelEx(&cfg, sgemm_kernel<BM, BN, kSgemmBK, TN, true>, a);
+            e = cudaLaunchKernelEx(&cfg, sgemm_kernel<Cfg, true>, a);
             if (e != cudaSuccess) return e;
         } else {
-            sgemm_kernel<BM, BN, kSgemmBK, TN, false>
-                <<<static_cast<unsigned>(part.tiles) * part.splits, kT, 0, stream>>>(a);
+            cudaError_t e = sgemm_prepare<Cfg, false>();
+            if (e != cudaSuccess) return e;
+            sgemm_kernel<Cfg, false><<<static_cast<unsigned>(part.tiles) * part.splits, Cfg::kThreads,
+                                       Cfg::kSmemBytes, stream>>>(a);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -628,36 +664,40 @@ __global__ void fill_scale_kernel(void* C, int ct, int64_t M, int64_t N, int64_t
 
 // ---------------------------------------------------------------- host --
 
-bool sgemm_tile_supported(int bm, int bn, int tn) {
-    if (tn == 16) return bm == 128 && bn == 128;
-    return tn == 8 && ((bm == 128 && bn == 128) || (bm == 128 && bn == 64) || (bm == 64 && bn == 64));
+// The SGEMM configurations built: (tile, micro-tile width).
+template <class F>
+static cudaError_t sgemm_dispatch(int bm, int bn, int tn, F&& f) {
+    if (bm == 128 && bn == 128 && tn == 16) return f(SgemmCfg<128, 128, kSgemmBK, 16>{});
+    if (bm == 128 && bn == 128 && tn == 8) return f(SgemmCfg<128, 128, kSgemmBK, 8>{});
+    if (bm == 128 && bn == 64 && tn == 8) return f(SgemmCfg<128, 64, kSgemmBK, 8>{});
+    if (bm == 64 && bn == 64 && tn == 8) return f(SgemmCfg<64, 64, kSgemmBK, 8>{});
+    return cudaErrorInvalidValue;
 }
 
-template <int BM, int BN, int TN>
-static cudaError_t blocks_per_sm(bool sk, int* n) {
-    constexpr int kT = SgemmCfg<BM, BN, kSgemmBK, TN>::kThreads;
-    return sk ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, TN, true>, kT, 0)
-              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<BM, BN, kSgemmBK, TN, false>, kT, 0);
+bool sgemm_tile_supported(int bm, int bn, int tn) {
+    return sgemm_dispatch(bm, bn, tn, [](auto) { return cudaSuccess; }) == cudaSuccess;
 }
 
 cudaError_t sgemm_blocks_per_sm(int bm, int bn, int tn, bool stream_k, int* n) {
-    if (tn == 16 && bm == 128 && bn == 128) return blocks_per_sm<128, 128, 16>(stream_k, n);
-    if (tn != 8) return cudaErrorInvalidValue;
-    if (bm == 128 && bn == 128) return blocks_per_sm<128, 128, 8>(stream_k, n);
-    if (bm == 128 && bn == 64) return blocks_per_sm<128, 64, 8>(stream_k, n);
-    if (bm == 64 && bn == 64) return blocks_per_sm<64, 64, 8>(stream_k, n);
-    return cudaErrorInvalidValue;
+    return sgemm_dispatch(bm, bn, tn, [&](auto c) {
+        using Cfg = decltype(c);
+        if (stream_k) {
+            cudaError_t e = sgemm_prepare<Cfg, true>();
+            if (e != cudaSuccess) return e;
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<Cfg, true>, Cfg::kThreads,
+                                                                 Cfg::kSmemBytes);
+        }
+        cudaError_t e = sgemm_prepare<Cfg, false>();
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, sgemm_kernel<Cfg, false>, Cfg::kThreads,
+                                                             Cfg::kSmemBytes);
+    });
 }
 
 int sgemm_k_step() { return kSgemmBK; }
 
 cudaError_t sgemm_launch(const SgemmLaunch& L, cudaStream_t stream) {
-    if (L.tn == 16 && L.bm == 128 && L.bn == 128) return sgemm_go<128, 128, 16>(L, stream);
-    if (L.tn != 8) return cudaErrorInvalidValue;
-    if (L.bm == 128 && L.bn == 128) return sgemm_go<128, 128, 8>(L, stream);
-    if (L.bm == 128 && L.bn == 64) return sgemm_go<128, 64, 8>(L, stream);
-    if (L.bm == 64 && L.bn == 64) return sgemm_go<64, 64, 8>(L, stream);
-    return cudaErrorInvalidValue;
+    return sgemm_dispatch(L.bm, L.bn, L.tn, [&](auto c) { return sgemm_go<decltype(c)>(L, stream); });
 }
 
 cudaError_t generic_launch(int dtype, const void* A, const void* B, void* C, int ct, int64_t M,

@@ -185,9 +185,9 @@ gemm_status_t gemm_e5m2f32_bt(const void *A, const void *Bt, float *C,
  *             stream-K (at the power cap, idle clusters in a partial last
  *             wave let the busy ones clock higher, which the measured shapes
  *             favour over the partial sums' traffic).  For the FP32 SGEMM it
- *             turns stream-K on when there are fewer than four waves of
+ *             turns stream-K on when there are fewer than three waves of
  *             128 x 128 tiles (M > 64), choosing the tile from the K steps
- *             each persistent CTA gets; from four waves on it runs whole
+ *             each persistent CTA gets; from three waves on it runs whole
  *             waves of 128 x 128 tiles with 8x16 outputs per thread (N > 64).
  *             Ignored with split_k > 0.
  *   epilogue  0 = C = A x B (alpha and beta ignored); 1 = C = alpha * (A x B)
